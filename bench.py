@@ -1,0 +1,366 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode-attention step on GB300.
+
+A step is one attention layer's decode step for the whole batch: the new
+tokens' K/V written into the paged cache (reshape_and_cache or quantize_kv),
+attention over every sequence's visible tokens (split-KV phase 1), and the
+log-sum-exp reduce.  The headline workload is the Llama-3-8B-like batch
+(batch 8, 32/8 heads, head_dim 128, bf16, ragged contexts 512..4096).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  `value` is algorithmic bytes (K + V + q + out +
+block tables + the write's bytes) per second of device time over the K timed
+steps; inputs are resident in HBM and rotate over enough replicas that the
+bytes touched between two uses of one replica exceed the L2 cache.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES_FALLBACK = 126 * 2 ** 20
+METRIC = "paged-decode attention KV-read GB/s (% of HBM peak); decode steps/sec"
+
+WORKLOADS = {
+    "tiny_f16": 1,
+    "llama3_8b_batch8": 2,
+    "long_context_32k": 3,
+    "k8v4_batch32": 4,
+    "verify_batch256": 5,
+}
+DEFAULT_WORKLOAD = "llama3_8b_batch8"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--partition", type=int, default=None, help="split-KV partition size (0 = single pass)")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle sample budget")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            for k in ("hbm_gbs", "hbm_GBs", "hbm_bandwidth_gbs"):
+                if k in d:
+                    return float(d[k]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def make_workload(name, device, seed_offset=0, partition=None):
+    from paged_decode_attention_cache_gb300 import workloads as W
+    fn = W.CONFIGS[WORKLOADS[name]]
+    kw = {}
+    if partition is not None and name != "tiny_f16":
+        kw["partition_size"] = partition
+    import inspect
+    sig = inspect.signature(fn)
+    seed = sig.parameters["seed"].default + seed_offset
+    w = fn(device=device, seed=seed, **kw) if "partition_size" in sig.parameters else fn(device=device, seed=seed)
+    if name == "tiny_f16" and partition is not None:
+        w.partition_size = partition
+    return w
+
+
+def step_bytes(w):
+    from paged_decode_attention_cache_gb300 import bytes_model as BM
+    ctx = [int(c) for c in w.context_lens.cpu()]
+    attn = BM.attention_bytes(ctx, w.q_len, w.num_heads, w.num_kv_heads, w.head_dim, w.cache)
+    wr = BM.write_bytes(int(w.slot_new.numel()), w.num_kv_heads, w.head_dim, w.cache)
+    return attn, wr
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_decode_attention_cache_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(workload, kernel):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel sources (null otherwise)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        e = d.get(f"{kernel}:{workload}")
+        if e and e.get("source_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        self.device_index = device_index
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.device_index), "-lms", "100"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, attn_bytes, budget_s):
+    """The oracle as it stands, on this host's cores, over whole steps of the
+    same workload until the time budget is spent (at least one step)."""
+    import numpy as np  # noqa: F401
+    from tests.helpers import oracle_attention, oracle_cache_after_step
+    threads = os.cpu_count() or 1
+    cs = oracle_cache_after_step(w)
+    import oracle
+    split = w.partition_size > 0
+    n, t0 = 0, time.perf_counter()
+    while True:
+        if split:   # phase 1 partials, then the LSE reduce, as the GPU step does
+            _, part = oracle_attention(w, cs, threads=threads, partition_size=w.partition_size,
+                                       max_partitions=w.max_partitions, want_out=False)
+            oracle.lse_reduce(*part)
+        else:
+            oracle_attention(w, cs, threads=threads)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or el / n * (n + 1) > 3 * budget_s:
+            break
+    per = el / n
+    return {"value": attn_bytes / per / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} full attention step(s) of {w.name} (fp64 scalar oracle: split-KV partials "
+                      f"+ LSE reduce when the step splits), {per:.3f} s each", "seconds_per_step": per}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = make_workload(args.workload, "cpu", 0, args.partition)
+    attn_b, wr_b = step_bytes(w)
+    cb = cpu_baseline(w, attn_b + wr_b, max(1.0, min(args.cpu_seconds, 20.0)))
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds_per_step"] * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": w.name},
+            "cpu_baseline": {k: cb[k] for k in ("kind", "cores", "sample", "value", "unit")},
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    from paged_decode_attention_cache_gb300 import build as pkv_build, ops
+    from paged_decode_attention_cache_gb300.runner import DecodeStep
+    if rank == 0 or ws == 1:
+        pkv_build.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    ops.lib()
+
+    w = make_workload(args.workload, dev, seed_offset=rank, partition=args.partition)
+    attn_b, wr_b = step_bytes(w)
+    total_b = attn_b + wr_b
+    l2 = getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_BYTES_FALLBACK
+    reps = max(2, math.ceil(3 * l2 / max(1, total_b)))
+    reps = min(reps, 16)
+    steps_ = [DecodeStep(w, dev) for _ in range(reps)]
+    stream = torch.cuda.current_stream()
+    launches = steps_[0].launches_per_step()
+
+    for i in range(max(3, args.warmup)):
+        steps_[i % reps].step()
+    torch.cuda.synchronize()
+    # hold the clocks under load for a moment so the sampler sees the loaded state
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_end = time.perf_counter() + 1.0
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(200):
+            steps_[i % reps].step()
+            i += 1
+        torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    start.record(stream)
+    for k in range(K):
+        st = steps_[k % reps]
+        st.write()
+        ev[k][0].record(stream)
+        st.attend_phase1()
+        ev[k][1].record(stream)
+        st.attend_phase2()
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    step_ms = start.elapsed_time(stop) / K
+    kern_ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    t = torch.tensor([step_ms, kern_ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    step_ms, kern_ms = float(t[0]), float(t[1])
+    flags = 0
+    for st in steps_:
+        flags |= st.error_flags()
+
+    # end to end through the same API with host buffers: pinned inputs copied in,
+    # the output copied back, every step
+    e2e = None
+    if not args.no_e2e:
+        st = steps_[0]
+        host_in = [x.cpu().pin_memory() for x in (st.q, st.k_new, st.v_new, st.slot_new,
+                                                   st.seqs.block_tables, st.seqs.context_lens)]
+        dev_in = [st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens]
+        host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        d2h = host_out.numel() * host_out.element_size()
+        Ke = max(10, min(K, 500))
+        for _ in range(3):
+            for hsrc, d in zip(host_in, dev_in):
+                d.copy_(hsrc, non_blocking=True)
+            st.step()
+            host_out.copy_(st.out, non_blocking=True)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(Ke):
+            for hsrc, d in zip(host_in, dev_in):
+                d.copy_(hsrc, non_blocking=True)
+            st.step()
+            host_out.copy_(st.out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / Ke
+        te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        if ws > 1:
+            torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(te[0])
+        e2e = {"value": ws * total_b / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    peak, peak_src = load_peaks()
+    achieved = attn_b / (kern_ms * 1e-3) / 1e9
+    kernel_name = "paged_attention_split" if steps_[0].split else "paged_attention"
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": traffic_from_profiles(w.name, kernel_name), "kernel": kernel_name,
+                "kernel_ms": kern_ms, "peak_source": f"{peak_src} (copy bandwidth)",
+                "frac_of_nominal_8000": achieved / 8000.0}
+    cb = None
+    if rank == 0 and not args.no_cpu_baseline:
+        wc = make_workload(args.workload, "cpu", 0, args.partition)
+        cb = cpu_baseline(wc, total_b, args.cpu_seconds)
+        cb.pop("seconds_per_step", None)
+
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return 0
+    value = ws * total_b / (step_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.num_seqs, "q_len": w.q_len, "heads": w.num_heads,
+                   "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "cache": w.cache,
+                   "partition_size": steps_[0].partition_size, "sum_context": int(w.context_lens.sum()),
+                   "bytes_per_step": total_b, "parallelism": f"replicas x{ws}",
+                   "l2": f"{reps} rotating input replicas, {reps * total_b / 2**20:.0f} MiB touched per cycle "
+                         f"vs {l2 / 2**20:.0f} MiB L2"},
+        "steps_per_s": 1e3 / step_ms * ws,
+        "tokens_per_s": 1e3 / step_ms * ws * w.num_seqs * w.q_len,
+        "roofline": roofline,
+        "cpu_baseline": cb,
+        "e2e": e2e,
+        "gpu_launches": K * launches,
+        "clocks": clocks,
+        "device_error_flags": flags,
+    }
+    print(json.dumps(line))
+    return 0 if flags == 0 else 3
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -217,7 +217,8 @@ int pkvo_gather_kv_cache(void *k_out, void *v_out, const int32_t *cu_seq_lens,
  *
  * Quantiser, as a fixed fp32 operation sequence:
  *   K: a = max_d |k_d|;  s = fp16_rne(a / 127);  c_d = s == 0 ? 0 : clamp(rint(k_d / s), -127, 127)
- *   V: lo = min, hi = max over the group;  s = fp16_rne((hi - lo) / 15);  z = fp16_rne(lo)
+ *   V: lo = min, hi = max over the group (a zero minimum taken as +0);
+ *      s = fp16_rne((hi - lo) / 15);  z = fp16_rne(lo)
  *      c_d = s == 0 ? 0 : clamp(rint((v_d - z) / s), 0, 15)
  * where rint rounds half to even and / is the IEEE-rounded fp32 quotient.
  * Dequantisation: k = c * s,  v = c * s + z. */
@@ -261,6 +262,7 @@ int pkvo_quantize_kv(int8_t *k_q, uint16_t *k_scale, uint8_t *v_q, uint16_t *v_s
                     if (kv[d] < lo) lo = kv[d];
                     if (kv[d] > hi) hi = kv[d];
                 }
+                if (lo == 0.0f) lo = 0.0f;            /* a zero minimum is stored as +0 */
                 uint16_t vs16 = pkvo_f32_to_f16_rne((hi - lo) / 15.0f);
                 uint16_t vz16 = pkvo_f32_to_f16_rne(lo);
                 float vs = (float)pkvo_f16_to_f64(vs16), vz = (float)pkvo_f16_to_f64(vz16);

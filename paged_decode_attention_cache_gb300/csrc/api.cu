@@ -1,0 +1,373 @@
+// api.cu -- the extern "C" boundary declared in include/pkv.h: host-side
+// argument checks, TMA tensor-map encoding and kernel dispatch.  Nothing here
+// allocates device memory and nothing is cached between calls.
+#include <cudaTypedefs.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "pkv.h"
+#include "pkv_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+pkv_status fail(pkv_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+pkv_status ok() {
+    g_last_error.clear();
+    return PKV_OK;
+}
+
+pkv_status cuda_result(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(PKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+#define CHECK_PTR(ptr, name)                                                                          \
+    do {                                                                                              \
+        if ((ptr) == nullptr) return fail(PKV_ERR_INVALID_ARG, "%s is NULL", name);                   \
+        if (!aligned16(ptr)) return fail(PKV_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);     \
+    } while (0)
+
+pkv_status check_cache(const pkv_cache* c, bool need_half) {
+    if (!c) return fail(PKV_ERR_INVALID_ARG, "cache is NULL");
+    if (c->kind != PKV_CACHE_F16 && c->kind != PKV_CACHE_BF16 && c->kind != PKV_CACHE_K8V4)
+        return fail(PKV_ERR_INVALID_ARG, "unknown cache kind %d", c->kind);
+    if (need_half && c->kind == PKV_CACHE_K8V4)
+        return fail(PKV_ERR_INVALID_ARG, "this call needs an fp16 or bf16 cache");
+    if (c->block_size != 16) return fail(PKV_ERR_UNSUPPORTED, "block_size %d (only 16)", c->block_size);
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(PKV_ERR_UNSUPPORTED, "head_dim %d (64 or 128)", c->head_dim);
+    if (c->num_kv_heads < 1 || c->num_kv_heads > 65535)
+        return fail(PKV_ERR_INVALID_ARG, "num_kv_heads %d", c->num_kv_heads);
+    if (c->num_blocks < 1 || int64_t(c->num_blocks) * 16 > INT32_MAX)
+        return fail(PKV_ERR_INVALID_ARG, "num_blocks %d", c->num_blocks);
+    CHECK_PTR(c->k, "cache->k");
+    CHECK_PTR(c->v, "cache->v");
+    if (c->kind == PKV_CACHE_K8V4) {
+        if (c->v_group != 32) return fail(PKV_ERR_UNSUPPORTED, "v_group %d (only 32)", c->v_group);
+        CHECK_PTR(c->k_scale, "cache->k_scale");
+        CHECK_PTR(c->v_scale, "cache->v_scale");
+        CHECK_PTR(c->v_zero, "cache->v_zero");
+    }
+    return PKV_OK;
+}
+
+pkv_status check_seqs(const pkv_seqs* s) {
+    if (!s) return fail(PKV_ERR_INVALID_ARG, "seqs is NULL");
+    if (s->num_seqs < 0 || s->num_seqs > 65535) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", s->num_seqs);
+    if (s->q_len < 1) return fail(PKV_ERR_INVALID_ARG, "q_len %d", s->q_len);
+    if (s->max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", s->max_blocks_per_seq);
+    if (int64_t(s->max_blocks_per_seq) * 16 > INT32_MAX / 2)
+        return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d too large", s->max_blocks_per_seq);
+    if (s->num_seqs > 0) {
+        if (!s->block_tables) return fail(PKV_ERR_INVALID_ARG, "seqs->block_tables is NULL");
+        if (!s->context_lens) return fail(PKV_ERR_INVALID_ARG, "seqs->context_lens is NULL");
+    }
+    return PKV_OK;
+}
+
+int cache_dtype(const pkv_cache* c) { return c->kind == PKV_CACHE_BF16 ? PKV_BF16 : PKV_F16; }
+
+// ---------------------------------------------------------------- tensor maps
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// A 2-D view of a paged cache tensor: rows = num_blocks*16 token slots, each
+// row `row_bytes` long; box = one kv head's `box_bytes` of 16 consecutive rows.
+pkv_status tile_map(CUtensorMap* map, void* base, int64_t rows, int64_t row_bytes, int box_bytes,
+                    CUtensorMapSwizzle swz) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t dims[2] = {cuuint64_t(row_bytes), cuuint64_t(rows)};
+    cuuint64_t strides[1] = {cuuint64_t(row_bytes)};
+    cuuint32_t box[2] = {cuuint32_t(box_bytes), 16u};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return PKV_OK;
+}
+
+pkv_status cache_maps(const pkv_cache* c, CUtensorMap* km, CUtensorMap* vm, bool swizzle_k) {
+    const int64_t rows = int64_t(c->num_blocks) * 16;
+    const int D = c->head_dim, H = c->num_kv_heads;
+    pkv_status st;
+    if (c->kind == PKV_CACHE_K8V4) {
+        st = tile_map(km, c->k, rows, int64_t(H) * D, D,
+                      swizzle_k && D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != PKV_OK) return st;
+        return tile_map(vm, c->v, rows, int64_t(H) * D / 2, D / 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    st = tile_map(km, c->k, rows, int64_t(H) * D * 2, D * 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != PKV_OK) return st;
+    return tile_map(vm, c->v, rows, int64_t(H) * D * 2, D * 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// Shared checks + parameter block of both attention entry points.
+pkv_status attn_setup(pkv::AttnParams* p, const void* q, pkv_dtype q_dtype, int32_t num_heads, float scale,
+                      const pkv_cache* cache, const pkv_seqs* seqs, uint32_t* err, int* gqa) {
+    pkv_status st = check_cache(cache, false);
+    if (st != PKV_OK) return st;
+    if ((st = check_seqs(seqs)) != PKV_OK) return st;
+    CHECK_PTR(q, "q");
+    if (q_dtype != PKV_F16 && q_dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "q_dtype %d", q_dtype);
+    if (cache->kind != PKV_CACHE_K8V4 && q_dtype != cache_dtype(cache))
+        return fail(PKV_ERR_INVALID_ARG, "q_dtype must match the fp16/bf16 cache dtype");
+    if (num_heads < 1 || num_heads % cache->num_kv_heads != 0)
+        return fail(PKV_ERR_INVALID_ARG, "num_heads %d is not a multiple of num_kv_heads %d", num_heads,
+                    cache->num_kv_heads);
+    *gqa = num_heads / cache->num_kv_heads;
+    if (*gqa != 1 && *gqa != 2 && *gqa != 4 && *gqa != 8)
+        return fail(PKV_ERR_UNSUPPORTED, "group size %d (1, 2, 4 or 8)", *gqa);
+    if (!(scale == scale)) return fail(PKV_ERR_INVALID_ARG, "scale is NaN");
+    const bool tc = seqs->q_len > 1 || cache->kind == PKV_CACHE_K8V4;
+    if (tc ? !pkv::decode_tc_supported(cache->kind, cache->head_dim, *gqa, seqs->q_len)
+           : !pkv::decode_cc_supported(cache->kind, cache->head_dim, *gqa))
+        return fail(PKV_ERR_UNSUPPORTED, "no kernel for cache kind %d, head_dim %d, group %d, q_len %d", cache->kind,
+                    cache->head_dim, *gqa, seqs->q_len);
+    *p = pkv::AttnParams{};
+    p->q = q;
+    p->q_dtype = q_dtype;
+    p->scale_log2 = scale * 1.4426950408889634f;
+    p->num_heads = num_heads;
+    p->num_kv_heads = cache->num_kv_heads;
+    p->q_len = seqs->q_len;
+    p->num_blocks = cache->num_blocks;
+    p->head_dim = cache->head_dim;
+    p->k_scale = cache->k_scale;
+    p->v_scale = cache->v_scale;
+    p->v_zero = cache->v_zero;
+    p->block_tables = seqs->block_tables;
+    p->context_lens = seqs->context_lens;
+    p->num_seqs = seqs->num_seqs;
+    p->max_blocks = seqs->max_blocks_per_seq;
+    p->err = err;
+    return PKV_OK;
+}
+
+pkv_status attn_launch(const pkv::AttnParams& p, const pkv_cache* cache, int gqa, int grid_parts,
+                       pkv_stream_t stream) {
+    const bool tc = p.q_len > 1 || cache->kind == PKV_CACHE_K8V4;
+    CUtensorMap km, vm;
+    pkv_status st = cache_maps(cache, &km, &vm, tc);
+    if (st != PKV_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = tc ? pkv::launch_decode_tc(p, cache->kind, gqa, km, vm, grid_parts, s)
+                       : pkv::launch_decode_cc(p, cache->kind, gqa, km, vm, grid_parts, s);
+    return cuda_result(e, "attention launch");
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_reshape_and_cache(const pkv_cache* cache, const void* k_new, const void* v_new,
+                                 const int64_t* slot_mapping, int32_t num_tokens, uint32_t* err_flags,
+                                 pkv_stream_t stream) {
+    pkv_status st = check_cache(cache, true);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+    if (num_tokens == 0) return ok();
+    CHECK_PTR(k_new, "k_new");
+    CHECK_PTR(v_new, "v_new");
+    if (!slot_mapping) return fail(PKV_ERR_INVALID_ARG, "slot_mapping is NULL");
+    pkv::CacheWriteParams p{};
+    p.k_cache = cache->k;
+    p.v_cache = cache->v;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
+    p.num_tokens = num_tokens;
+    p.num_blocks = cache->num_blocks;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.head_dim = cache->head_dim;
+    p.err = err_flags;
+    return cuda_result(pkv::launch_reshape_and_cache(p, 2, reinterpret_cast<cudaStream_t>(stream)),
+                       "reshape_and_cache launch");
+}
+
+pkv_status pkv_quantize_kv(const pkv_cache* cache, const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                           const int64_t* slot_mapping, int32_t num_tokens, uint32_t* err_flags,
+                           pkv_stream_t stream) {
+    pkv_status st = check_cache(cache, false);
+    if (st != PKV_OK) return st;
+    if (cache->kind != PKV_CACHE_K8V4) return fail(PKV_ERR_INVALID_ARG, "quantize_kv needs a K8V4 cache");
+    if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "src_dtype %d", src_dtype);
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+    if (num_tokens == 0) return ok();
+    CHECK_PTR(k_new, "k_new");
+    CHECK_PTR(v_new, "v_new");
+    if (!slot_mapping) return fail(PKV_ERR_INVALID_ARG, "slot_mapping is NULL");
+    pkv::CacheWriteParams p{};
+    p.k_cache = cache->k;
+    p.v_cache = cache->v;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
+    p.num_tokens = num_tokens;
+    p.num_blocks = cache->num_blocks;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.head_dim = cache->head_dim;
+    p.err = err_flags;
+    p.k_scale = cache->k_scale;
+    p.v_scale = cache->v_scale;
+    p.v_zero = cache->v_zero;
+    p.src_dtype = src_dtype;
+    return cuda_result(pkv::launch_quantize_kv(p, reinterpret_cast<cudaStream_t>(stream)), "quantize_kv launch");
+}
+
+pkv_status pkv_paged_attention(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype, int32_t num_heads,
+                               float scale, const pkv_cache* cache, const pkv_seqs* seqs, uint32_t* err_flags,
+                               pkv_stream_t stream) {
+    pkv::AttnParams p;
+    int gqa = 0;
+    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
+    if (st != PKV_OK) return st;
+    CHECK_PTR(out, "out");
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+        return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (seqs->num_seqs == 0) return ok();
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.partition_blocks = seqs->max_blocks_per_seq;
+    p.max_partitions = 1;
+    return attn_launch(p, cache, gqa, 1, stream);
+}
+
+size_t pkv_split_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t head_dim, int32_t max_partitions) {
+    if (num_rows <= 0 || num_heads <= 0 || head_dim <= 0 || max_partitions <= 0) return 0;
+    const size_t n = size_t(num_rows) * size_t(num_heads) * size_t(max_partitions);
+    return align256(n * size_t(head_dim) * 4) + 2 * align256(n * 4);
+}
+
+pkv_status pkv_paged_attention_split(float* tmp_out, float* max_logits, float* exp_sums, int32_t partition_size,
+                                     int32_t max_partitions, const void* q, pkv_dtype q_dtype, int32_t num_heads,
+                                     float scale, const pkv_cache* cache, const pkv_seqs* seqs,
+                                     uint32_t* err_flags, pkv_stream_t stream) {
+    pkv::AttnParams p;
+    int gqa = 0;
+    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
+    if (st != PKV_OK) return st;
+    CHECK_PTR(tmp_out, "tmp_out");
+    CHECK_PTR(max_logits, "max_logits");
+    CHECK_PTR(exp_sums, "exp_sums");
+    if (partition_size < 16 || partition_size % 16 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "partition_size %d is not a positive multiple of 16", partition_size);
+    if (max_partitions < 1 || max_partitions > 65535)
+        return fail(PKV_ERR_INVALID_ARG, "max_partitions %d", max_partitions);
+    if (int64_t(max_partitions) * partition_size < int64_t(seqs->max_blocks_per_seq) * 16)
+        return fail(PKV_ERR_INVALID_ARG, "max_partitions * partition_size (%lld) does not cover the block table (%lld)",
+                    (long long)max_partitions * partition_size, (long long)seqs->max_blocks_per_seq * 16);
+    if (seqs->num_seqs == 0) return ok();
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.partition_blocks = partition_size / 16;
+    p.max_partitions = max_partitions;
+    const int grid_parts = int((int64_t(seqs->max_blocks_per_seq) * 16 + partition_size - 1) / partition_size);
+    return attn_launch(p, cache, gqa, grid_parts, stream);
+}
+
+pkv_status pkv_reduce(void* out, pkv_dtype out_dtype, const float* tmp_out, const float* max_logits,
+                      const float* exp_sums, const pkv_seqs* seqs, int32_t num_heads, int32_t head_dim,
+                      int32_t partition_size, int32_t max_partitions, pkv_stream_t stream) {
+    pkv_status st = check_seqs(seqs);
+    if (st != PKV_OK) return st;
+    CHECK_PTR(out, "out");
+    CHECK_PTR(tmp_out, "tmp_out");
+    CHECK_PTR(max_logits, "max_logits");
+    CHECK_PTR(exp_sums, "exp_sums");
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+        return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (head_dim != 64 && head_dim != 128) return fail(PKV_ERR_UNSUPPORTED, "head_dim %d", head_dim);
+    if (num_heads < 1) return fail(PKV_ERR_INVALID_ARG, "num_heads %d", num_heads);
+    if (partition_size < 16 || partition_size % 16 != 0)
+        return fail(PKV_ERR_INVALID_ARG, "partition_size %d", partition_size);
+    if (max_partitions < 1) return fail(PKV_ERR_INVALID_ARG, "max_partitions %d", max_partitions);
+    if (seqs->num_seqs == 0) return ok();
+    if (int64_t(seqs->num_seqs) * seqs->q_len > INT32_MAX) return fail(PKV_ERR_INVALID_ARG, "too many rows");
+    pkv::ReduceParams p{};
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.tmp_out = tmp_out;
+    p.max_logits = max_logits;
+    p.exp_sums = exp_sums;
+    p.context_lens = seqs->context_lens;
+    p.num_seqs = seqs->num_seqs;
+    p.q_len = seqs->q_len;
+    p.num_heads = num_heads;
+    p.head_dim = head_dim;
+    p.partition_size = partition_size;
+    p.max_partitions = max_partitions;
+    return cuda_result(pkv::launch_reduce(p, reinterpret_cast<cudaStream_t>(stream)), "reduce launch");
+}
+
+pkv_status pkv_gather_kv_cache(void* k_out, void* v_out, const int32_t* cu_seq_lens, const pkv_cache* cache,
+                               const pkv_seqs* seqs, uint32_t* err_flags, pkv_stream_t stream) {
+    pkv_status st = check_cache(cache, true);
+    if (st != PKV_OK) return st;
+    if ((st = check_seqs(seqs)) != PKV_OK) return st;
+    if (seqs->num_seqs == 0) return ok();
+    CHECK_PTR(k_out, "k_out");
+    CHECK_PTR(v_out, "v_out");
+    if (!cu_seq_lens) return fail(PKV_ERR_INVALID_ARG, "cu_seq_lens is NULL");
+    pkv::GatherParams p{};
+    p.k_out = k_out;
+    p.v_out = v_out;
+    p.cu_seq_lens = cu_seq_lens;
+    p.k_cache = cache->k;
+    p.v_cache = cache->v;
+    p.block_tables = seqs->block_tables;
+    p.context_lens = seqs->context_lens;
+    p.num_seqs = seqs->num_seqs;
+    p.max_blocks = seqs->max_blocks_per_seq;
+    p.num_blocks = cache->num_blocks;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.head_dim = cache->head_dim;
+    p.err = err_flags;
+    return cuda_result(pkv::launch_gather(p, 2, reinterpret_cast<cudaStream_t>(stream)), "gather launch");
+}
+
+const char* pkv_status_string(pkv_status status) {
+    switch (status) {
+        case PKV_OK: return "ok";
+        case PKV_ERR_INVALID_ARG: return "invalid argument";
+        case PKV_ERR_UNSUPPORTED: return "unsupported shape or type";
+        case PKV_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+const char* pkv_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,213 @@
+// cache_ops.cu -- writes into and reads out of the paged cache:
+//   reshape_and_cache  scatter new K/V rows into their slots (bit-exact copy)
+//   gather_kv_cache    copy each sequence's visible tokens back to contiguous rows
+//   quantize_kv        K int8 symmetric + V 4-bit asymmetric write path
+// All three are pure data movement bounded by HBM: 16-byte vector accesses,
+// consecutive threads on consecutive 16-byte chunks of a token row.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kBlockSize = 16;
+constexpr int kThreads = 256;
+
+// ---------------------------------------------------------------- reshape_and_cache
+// [mlxcel manual "KV Cache", §"Attention Dispatch and In-Place Decode Writes":
+//  the new row is written straight into the cache buffer; metalworking "The KV
+//  Cache" names the reshape_and_cache kernel.]  One token's K (or V) row across
+// all kv heads is contiguous in both the source [T, Hkv, D] and the cache
+// [NB, 16, Hkv, D], so each token is `chunks` 16-byte chunks copied verbatim.
+__global__ void __launch_bounds__(kThreads) reshape_and_cache_kernel(CacheWriteParams p, int chunks) {
+    const int64_t total = int64_t(p.num_tokens) * chunks;
+    const int64_t pool = int64_t(p.num_blocks) * kBlockSize;
+    for (int64_t i = blockIdx.x * int64_t(kThreads) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * kThreads) {
+        const int64_t tok = i / chunks;
+        const int c = int(i - tok * chunks);
+        const int64_t slot = p.slot_mapping[tok];
+        if (slot < 0) continue;  // padding
+        if (slot >= pool) {
+            if (c == 0) flag_error(p.err, PKV_DEVERR_OOB_SLOT);
+            continue;
+        }
+        const uint4* ks = reinterpret_cast<const uint4*>(p.k_new) + tok * chunks + c;
+        const uint4* vs = reinterpret_cast<const uint4*>(p.v_new) + tok * chunks + c;
+        uint4* kd = reinterpret_cast<uint4*>(p.k_cache) + slot * chunks + c;
+        uint4* vd = reinterpret_cast<uint4*>(p.v_cache) + slot * chunks + c;
+        *kd = __ldg(ks);
+        *vd = __ldg(vs);
+    }
+}
+
+// ---------------------------------------------------------------- gather_kv_cache
+// [metalworking "The KV Cache": fixed-size blocks plus an indirection table;
+//  gather_kv_cache names the read back to contiguous storage.]  CTA (b, s)
+// copies logical block b of sequence s.
+__global__ void __launch_bounds__(kThreads) gather_kernel(GatherParams p, int chunks) {
+    const int s = blockIdx.y, b = blockIdx.x;
+    int ctx = p.context_lens[s];
+    const int cap = p.max_blocks * kBlockSize;
+    if (ctx > cap) {
+        if (b == 0 && threadIdx.x == 0) flag_error(p.err, PKV_DEVERR_CAPACITY);
+        ctx = cap;
+    }
+    const int t0 = b * kBlockSize;
+    if (t0 >= ctx) return;
+    const int ntok = min(kBlockSize, ctx - t0);
+    const int pb = p.block_tables[int64_t(s) * p.max_blocks + b];
+    if (pb < 0 || pb >= p.num_blocks) {
+        if (threadIdx.x == 0) flag_error(p.err, PKV_DEVERR_OOB_BLOCK);
+        return;
+    }
+    const int64_t dst_row0 = int64_t(p.cu_seq_lens[s]) + t0;
+    const uint4* ksrc = reinterpret_cast<const uint4*>(p.k_cache) + int64_t(pb) * kBlockSize * chunks;
+    const uint4* vsrc = reinterpret_cast<const uint4*>(p.v_cache) + int64_t(pb) * kBlockSize * chunks;
+    uint4* kdst = reinterpret_cast<uint4*>(p.k_out) + dst_row0 * chunks;
+    uint4* vdst = reinterpret_cast<uint4*>(p.v_out) + dst_row0 * chunks;
+    const int n = ntok * chunks;  // the block's first ntok token rows are contiguous
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        kdst[i] = __ldg(ksrc + i);
+        vdst[i] = __ldg(vsrc + i);
+    }
+}
+
+// ---------------------------------------------------------------- quantize_kv
+// [metalworking "The KV Cache", §"The K/V asymmetry": K stays at 8 bits, V goes
+//  to 4; MTPLX "How MTPLX Manages Memory with KV Caching Strategies", the
+//  quantised write path with per-block scale and zero tensors.]  One warp per
+// (token, kv head).  The fp32 operation sequence is fixed so that codes and
+// scales are reproducible bit for bit: IEEE division (__fdiv_rn), IEEE
+// subtraction (__fsub_rn, never contracted), round-half-even (rintf), and RNE
+// conversion of scales to fp16 before they are used.
+template <typename Src, int D>
+__global__ void __launch_bounds__(kThreads) quantize_kernel(CacheWriteParams p) {
+    constexpr int E = D / 32;            // values per lane
+    constexpr int kGroup = 32;           // V group size along head_dim
+    constexpr int NG = D / kGroup;       // groups per row
+    constexpr int LPG = kGroup / E;      // lanes per group
+    const int lane = threadIdx.x & 31;
+    const int64_t w = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+    const int H = p.num_kv_heads;
+    if (w >= int64_t(p.num_tokens) * H) return;
+    const int64_t tok = w / H;
+    const int h = int(w - tok * H);
+    const int64_t slot = p.slot_mapping[tok];
+    if (slot < 0) return;
+    if (slot >= int64_t(p.num_blocks) * kBlockSize) {
+        if (lane == 0) flag_error(p.err, PKV_DEVERR_OOB_SLOT);
+        return;
+    }
+    const int64_t blk = slot / kBlockSize;
+    const int off = int(slot - blk * kBlockSize);
+    const int64_t src = (tok * H + h) * D + lane * E;
+    const uint16_t* ksrc = reinterpret_cast<const uint16_t*>(p.k_new) + src;
+    const uint16_t* vsrc = reinterpret_cast<const uint16_t*>(p.v_new) + src;
+    float k[E], v[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        k[e] = Half16<Src>::to_float(ksrc[e]);
+        v[e] = Half16<Src>::to_float(vsrc[e]);
+    }
+    // K: symmetric int8, one fp16 scale per (token, kv head)
+    float a = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) a = fmaxf(a, fabsf(k[e]));
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const __half s16 = __float2half_rn(__fdiv_rn(a, 127.0f));
+    const float s = __half2float(s16);
+    uint32_t kpack = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float c = (s == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(k[e], s)), -127.f), 127.f);
+        kpack |= (uint32_t(int32_t(c)) & 0xffu) << (8 * e);
+    }
+    const int64_t row = (blk * kBlockSize + off) * H + h;
+    const int64_t meta = (blk * H + h) * kBlockSize + off;
+    int8_t* kq = reinterpret_cast<int8_t*>(p.k_cache) + row * D + lane * E;
+    if constexpr (E == 4)
+        *reinterpret_cast<uint32_t*>(kq) = kpack;
+    else
+        *reinterpret_cast<uint16_t*>(kq) = uint16_t(kpack);
+    if (lane == 0) reinterpret_cast<__half*>(p.k_scale)[meta] = s16;
+
+    // V: asymmetric 4-bit per group of 32 dims, fp16 scale and fp16 zero per group
+    float lo = v[0], hi = v[0];
+#pragma unroll
+    for (int e = 1; e < E; ++e) {
+        lo = fminf(lo, v[e]);
+        hi = fmaxf(hi, v[e]);
+    }
+#pragma unroll
+    for (int o = LPG / 2; o >= 1; o >>= 1) {
+        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lo == 0.f) lo = 0.f;  // a zero minimum is stored as +0
+    const __half vs16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
+    const __half vz16 = __float2half_rn(lo);
+    const float vs = __half2float(vs16), vz = __half2float(vz16);
+    uint32_t vpack = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float c = (vs == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[e], vz), vs)), 0.f), 15.f);
+        vpack |= uint32_t(c) << (4 * e);  // even dim in the low nibble
+    }
+    uint8_t* vq = reinterpret_cast<uint8_t*>(p.v_cache) + row * (D / 2) + lane * (E / 2);
+    if constexpr (E == 4)
+        *reinterpret_cast<uint16_t*>(vq) = uint16_t(vpack);
+    else
+        *vq = uint8_t(vpack);
+    const int g = lane / LPG;
+    if (lane % LPG == 0) {
+        reinterpret_cast<__half*>(p.v_scale)[meta * NG + g] = vs16;
+        reinterpret_cast<__half*>(p.v_zero)[meta * NG + g] = vz16;
+    }
+}
+
+int grid_for(int64_t work, int per_cta) {
+    int64_t g = (work + per_cta - 1) / per_cta;
+    if (g < 1) g = 1;
+    if (g > 152 * 16) g = 152 * 16;
+    return int(g);
+}
+
+}  // namespace
+
+cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, int elem_bytes, cudaStream_t stream) {
+    const int chunks = p.num_kv_heads * p.head_dim * elem_bytes / 16;
+    reshape_and_cache_kernel<<<grid_for(int64_t(p.num_tokens) * chunks, kThreads), kThreads, 0, stream>>>(p, chunks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const GatherParams& p, int elem_bytes, cudaStream_t stream) {
+    const int chunks = p.num_kv_heads * p.head_dim * elem_bytes / 16;
+    dim3 grid(p.max_blocks, p.num_seqs);
+    gather_kernel<<<grid, kThreads, 0, stream>>>(p, chunks);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_kv(const CacheWriteParams& p, cudaStream_t stream) {
+    const int64_t warps = int64_t(p.num_tokens) * p.num_kv_heads;
+    const int64_t g64 = (warps * 32 + kThreads - 1) / kThreads;
+    if (g64 > 0x7fffffff) return cudaErrorInvalidValue;
+    const int grid = int(g64 < 1 ? 1 : g64);
+    const bool bf = p.src_dtype == PKV_BF16;
+    if (p.head_dim == 128) {
+        if (bf)
+            quantize_kernel<__nv_bfloat16, 128><<<grid, kThreads, 0, stream>>>(p);
+        else
+            quantize_kernel<__half, 128><<<grid, kThreads, 0, stream>>>(p);
+    } else {
+        if (bf)
+            quantize_kernel<__nv_bfloat16, 64><<<grid, kThreads, 0, stream>>>(p);
+        else
+            quantize_kernel<__half, 64><<<grid, kThreads, 0, stream>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,101 @@
+"""One decode step of the paged attention path on the GPU, for a seeded workload.
+
+A step is what one attention layer does per decode step: write the new
+tokens' K/V into their cache slots (reshape_and_cache, or quantize_kv for the
+K8/V4 cache), then attention over every sequence's visible tokens, either
+single pass or split-KV followed by the log-sum-exp reduce.  All device
+memory is allocated here by torch, once; the library itself allocates nothing.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import ops
+from .workloads import Workload
+
+_TORCH = {"f16": torch.float16, "bf16": torch.bfloat16}
+F16_NAN = 0x7E00
+
+
+class DecodeStep:
+    def __init__(self, w: Workload, device: str = "cuda", partition_size: Optional[int] = None,
+                 out_dtype: Optional[torch.dtype] = None):
+        self.w = w
+        self.device = device
+        dev = torch.device(device)
+        self.partition_size = w.partition_size if partition_size is None else partition_size
+        self.seqs = ops.Seqs(w.block_tables.to(dev).contiguous(), w.context_lens.to(dev).contiguous(), w.q_len)
+        self.q = w.q.to(dev).contiguous()
+        self.k_new = w.k_new.to(dev).contiguous()
+        self.v_new = w.v_new.to(dev).contiguous()
+        self.slot_new = w.slot_new.to(dev).contiguous()
+        self.err = torch.zeros(1, dtype=torch.int32, device=dev)
+        if w.cache == "k8v4":
+            self.cache = ops.Cache.empty("k8v4", w.num_blocks, w.num_kv_heads, w.head_dim, device=dev)
+            nan = torch.tensor(F16_NAN, dtype=torch.int16).view(torch.float16).item()
+            # slots never written keep NaN scales, so a stray read poisons the output
+            self.cache.k_scale.fill_(nan)
+            self.cache.v_scale.fill_(nan)
+            self.cache.v_zero.fill_(nan)
+            if w.k_hist is not None and w.k_hist.shape[0]:
+                ops.pkv_quantize_kv(self.cache, w.k_hist.to(dev).contiguous(), w.v_hist.to(dev).contiguous(),
+                                    w.slot_hist.to(dev).contiguous(), self.err)
+        else:
+            self.cache = ops.Cache(w.cache, w.k_cache.to(dev).contiguous().clone(),
+                                   w.v_cache.to(dev).contiguous().clone())
+        dt = out_dtype or _TORCH[w.src_dtype]
+        self.out = torch.empty((w.num_rows, w.num_heads, w.head_dim), dtype=dt, device=dev)
+        if self.partition_size > 0:
+            nparts = -(-w.max_blocks * 16 // self.partition_size)
+            self.ws = ops.split_workspace(w.num_rows, w.num_heads, w.head_dim, nparts, device=dev)
+        else:
+            self.ws = None
+
+    @property
+    def split(self) -> bool:
+        return self.ws is not None
+
+    def write(self, stream=None):
+        if self.k_new.shape[0] == 0:
+            return
+        if self.w.cache == "k8v4":
+            ops.pkv_quantize_kv(self.cache, self.k_new, self.v_new, self.slot_new, self.err, stream)
+        else:
+            ops.pkv_reshape_and_cache(self.cache, self.k_new, self.v_new, self.slot_new, self.err, stream)
+
+    def attend_phase1(self, stream=None):
+        """The dominant kernel: single-pass attention, or split-KV phase 1."""
+        if self.split:
+            tmp, ml, es = self.ws
+            ops.pkv_paged_attention_split(tmp, ml, es, self.partition_size, self.q, self.w.scale, self.cache,
+                                          self.seqs, self.err, stream)
+        else:
+            ops.pkv_paged_attention(self.out, self.q, self.w.scale, self.cache, self.seqs, self.err, stream)
+
+    def attend_phase2(self, stream=None):
+        if self.split:
+            tmp, ml, es = self.ws
+            ops.pkv_reduce(self.out, tmp, ml, es, self.seqs, self.partition_size, stream)
+
+    def step(self, stream=None) -> torch.Tensor:
+        self.write(stream)
+        self.attend_phase1(stream)
+        self.attend_phase2(stream)
+        return self.out
+
+    def launches_per_step(self) -> int:
+        return int(self.k_new.shape[0] > 0) + 1 + int(self.split)
+
+    def gather(self, stream=None):
+        cu = self.w.cu_seq_lens().to(self.seqs.context_lens.device)
+        total = int(cu[-1])
+        k_out = torch.empty((total, self.w.num_kv_heads, self.w.head_dim), dtype=self.cache.k.dtype,
+                            device=self.cache.k.device)
+        v_out = torch.empty_like(k_out)
+        ops.pkv_gather_kv_cache(k_out, v_out, cu, self.cache, self.seqs, self.err, stream)
+        return k_out, v_out
+
+    def error_flags(self) -> int:
+        return int(self.err.item())
