@@ -116,19 +116,29 @@ pkv_status tile_map(CUtensorMap* map, void* base, int64_t rows, int64_t row_byte
     return PKV_OK;
 }
 
-pkv_status cache_maps(const pkv_cache* c, CUtensorMap* km, CUtensorMap* vm, bool swizzle_k) {
+CUtensorMapSwizzle swizzle_for(int row_bytes) {
+    return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                            : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+// CUDA-core kernel: one box per tile (16 rows x one kv head), no swizzle.
+// Tensor-core kernel: swizzled boxes of at most 128 bytes per row, so that the
+// ldmatrix / 128-bit reads of a tile are conflict-free (fp16/bf16: 64-dim boxes
+// with the 128B swizzle; K8: the whole D-byte row; V4: the whole D/2-byte row).
+pkv_status cache_maps(const pkv_cache* c, CUtensorMap* km, CUtensorMap* vm, bool tc) {
     const int64_t rows = int64_t(c->num_blocks) * 16;
     const int D = c->head_dim, H = c->num_kv_heads;
     pkv_status st;
     if (c->kind == PKV_CACHE_K8V4) {
-        st = tile_map(km, c->k, rows, int64_t(H) * D, D,
-                      swizzle_k && D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
+        st = tile_map(km, c->k, rows, int64_t(H) * D, D, swizzle_for(D));
         if (st != PKV_OK) return st;
-        return tile_map(vm, c->v, rows, int64_t(H) * D / 2, D / 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+        return tile_map(vm, c->v, rows, int64_t(H) * D / 2, D / 2, swizzle_for(D / 2));
     }
-    st = tile_map(km, c->k, rows, int64_t(H) * D * 2, D * 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    const int box = tc ? 128 : D * 2;
+    const CUtensorMapSwizzle swz = tc ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
+    st = tile_map(km, c->k, rows, int64_t(H) * D * 2, box, swz);
     if (st != PKV_OK) return st;
-    return tile_map(vm, c->v, rows, int64_t(H) * D * 2, D * 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+    return tile_map(vm, c->v, rows, int64_t(H) * D * 2, box, swz);
 }
 
 // Shared checks + parameter block of both attention entry points.

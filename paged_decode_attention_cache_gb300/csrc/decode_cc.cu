@@ -53,7 +53,8 @@ struct CC {
     static constexpr int OFF_BAR = S * STAGE;
     static constexpr int OFF_POISON = OFF_BAR + 2 * S * 8;
     static constexpr int OFF_SC = align_up(OFF_POISON + S * 4, 16);
-    static constexpr int OFF_ALPHA = OFF_SC + NCW * kBS * G * 4;
+    static constexpr int OFF_PC = OFF_SC + NCW * kBS * G * 4;          // (p, p) pairs
+    static constexpr int OFF_ALPHA = OFF_PC + NCW * kBS * G * 8;
     static constexpr int OFF_MW = OFF_ALPHA + NCW * G * 4;
     static constexpr int OFF_LW = OFF_MW + NCW * G * 4;
     static constexpr int OFF_ACC = align_up(OFF_LW + NCW * G * 4, 16);
@@ -74,6 +75,20 @@ __device__ __forceinline__ void load_p(const float* src, float (&p)[N]) {
     } else if constexpr (N == 2) {
         const float2 v = *reinterpret_cast<const float2*>(src);
         p[0] = v.x; p[1] = v.y;
+    } else {
+        p[0] = src[0];
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void load_p2(const float2* src, float2 (&p)[N]) {
+    if constexpr (N >= 2) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            const float4 v = *reinterpret_cast<const float4*>(src + i);
+            p[i] = make_float2(v.x, v.y);
+            p[i + 1] = make_float2(v.z, v.w);
+        }
     } else {
         p[0] = src[0];
     }
@@ -160,7 +175,8 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 
     // ---------------------------------------------------------------- consumers
     const int grp = lane / C::LPT, jl = lane % C::LPT;
-    float qf[G][C::CPL * 8];
+    // q in registers as (even, odd) dim pairs, pre-scaled by scale*log2(e)
+    float2 q2[G][C::CPL * 4];
     {
         const T* qrow = reinterpret_cast<const T*>(p.q) + (size_t(r) * H + kvh * G) * D;
 #pragma unroll
@@ -172,18 +188,25 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float2 f = Half16<T>::unpack2(wds[i]);
-                    qf[h][k * 8 + 2 * i] = f.x * p.scale_log2;
-                    qf[h][k * 8 + 2 * i + 1] = f.y * p.scale_log2;
+                    q2[h][k * 4 + i] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
                 }
             }
     }
+    // the head whose score this lane holds after the reduce-scatter of the QK sums
+    int my_head = 0;
+#pragma unroll
+    for (int o = C::LPT / 2, nv = G; nv > 1; o >>= 1, nv >>= 1)
+        if (jl & o) my_head += nv / 2;
+    const bool writer = (jl & (C::LPT / G - 1)) == 0;
+
     float m_run = -INFINITY, l_run = 0.f;  // for head lane % G
-    float acc[G][C::DPL];
+    float2 acc[G][C::DPL / 2];
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int e = 0; e < C::DPL; ++e) acc[h][e] = 0.f;
+        for (int e = 0; e < C::DPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
     float* sc = reinterpret_cast<float*>(smem + C::OFF_SC) + warp * kBS * G;
+    float2* pc = reinterpret_cast<float2*>(smem + C::OFF_PC) + warp * kBS * G;
     float* alph = reinterpret_cast<float*>(smem + C::OFF_ALPHA) + warp * G;
 
     for (int j = warp; j < nblk; j += NCW) {
@@ -200,9 +223,9 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 #pragma unroll
             for (int pass = 0; pass < C::NPASS; ++pass) {
                 const int t = pass * C::TPP + grp;
-                float a[G];
+                float2 a2[G];
 #pragma unroll
-                for (int h = 0; h < G; ++h) a[h] = 0.f;
+                for (int h = 0; h < G; ++h) a2[h] = make_float2(0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < C::CPL; ++k) {
                     const uint4 raw = *reinterpret_cast<const uint4*>(Ks + t * D + (jl + k * C::LPT) * 8);
@@ -211,20 +234,29 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                     for (int i = 0; i < 4; ++i) {
                         const float2 f = Half16<T>::unpack2(wds[i]);
 #pragma unroll
-                        for (int h = 0; h < G; ++h) {
-                            a[h] = fmaf(qf[h][k * 8 + 2 * i], f.x, a[h]);
-                            a[h] = fmaf(qf[h][k * 8 + 2 * i + 1], f.y, a[h]);
-                        }
+                        for (int h = 0; h < G; ++h) a2[h] = __ffma2_rn(q2[h][k * 4 + i], f, a2[h]);
                     }
                 }
+                float a[G];
 #pragma unroll
-                for (int o = C::LPT / 2; o >= 1; o >>= 1)
+                for (int h = 0; h < G; ++h) a[h] = a2[h].x + a2[h].y;
+                // reduce-scatter over the LPT lanes of the token: halve the live heads per level
 #pragma unroll
-                    for (int h = 0; h < G; ++h) a[h] += __shfl_xor_sync(0xffffffffu, a[h], o);
-                if (jl == 0) {
+                for (int o = C::LPT / 2, nv = G; o >= 1; o >>= 1) {
+                    const bool up = (jl & o) != 0;
+                    if (nv > 1) {
 #pragma unroll
-                    for (int h = 0; h < G; ++h) sc[t * G + h] = (t < ntok) ? a[h] : -INFINITY;
+                        for (int i = 0; i < nv / 2; ++i) {
+                            const float send = up ? a[i] : a[i + nv / 2];
+                            const float keep = up ? a[i + nv / 2] : a[i];
+                            a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                        }
+                        nv >>= 1;
+                    } else {
+                        a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
+                    }
                 }
+                if (writer) sc[t * G + my_head] = (t < ntok) ? a[0] : -INFINITY;
             }
             __syncwarp();
             // ---- online softmax over the block's 16 x G scores
@@ -247,7 +279,7 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 const int e = lane + 32 * i;
                 const float pe = exp2f(x[i] - m_new);
                 bsum += pe;
-                if (e < NE) sc[e] = pe;
+                if (e < NE) pc[e] = make_float2(pe, pe);
             }
 #pragma unroll
             for (int o = G; o < 32; o <<= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, o);
@@ -263,28 +295,30 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 #pragma unroll
                 for (int h = 0; h < G; ++h)
 #pragma unroll
-                    for (int e = 0; e < C::DPL; ++e) acc[h][e] *= alv[h];
+                    for (int e = 0; e < C::DPL / 2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alv[h], alv[h]));
             }
-#pragma unroll
-            for (int t = 0; t < kBS; ++t) {
-                if (t < ntok) {
-                    float vf[C::DPL];
-                    if constexpr (C::DPL == 4) {
-                        const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * D + lane * 4);
-                        const float2 f0 = Half16<T>::unpack2(raw.x), f1 = Half16<T>::unpack2(raw.y);
-                        vf[0] = f0.x; vf[1] = f0.y; vf[2] = f1.x; vf[3] = f1.y;
-                    } else {
-                        const uint32_t raw = *reinterpret_cast<const uint32_t*>(Vs + t * D + lane * 2);
-                        const float2 f0 = Half16<T>::unpack2(raw);
-                        vf[0] = f0.x; vf[1] = f0.y;
-                    }
-                    float pv[G];
-                    load_p<G>(sc + t * G, pv);
-#pragma unroll
-                    for (int h = 0; h < G; ++h)
-#pragma unroll
-                        for (int e = 0; e < C::DPL; ++e) acc[h][e] = fmaf(pv[h], vf[e], acc[h][e]);
+            auto pv_token = [&](int t) {
+                float2 vf[C::DPL / 2];
+                if constexpr (C::DPL == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * D + lane * 4);
+                    vf[0] = Half16<T>::unpack2(raw.x);
+                    vf[1] = Half16<T>::unpack2(raw.y);
+                } else {
+                    vf[0] = Half16<T>::unpack2(*reinterpret_cast<const uint32_t*>(Vs + t * D + lane * 2));
                 }
+                float2 pp[G];
+                load_p2<G>(pc + t * G, pp);
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+#pragma unroll
+                    for (int e = 0; e < C::DPL / 2; ++e) acc[h][e] = __ffma2_rn(pp[h], vf[e], acc[h][e]);
+            };
+            if (ntok == kBS) {
+#pragma unroll
+                for (int t = 0; t < kBS; ++t) pv_token(t);
+            } else {
+#pragma unroll 1
+                for (int t = 0; t < ntok; ++t) pv_token(t);
             }
         }
         __syncwarp();
@@ -302,7 +336,8 @@ decode_cc_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 #pragma unroll
     for (int h = 0; h < G; ++h)
 #pragma unroll
-        for (int e = 0; e < C::DPL; ++e) accw[(warp * G + h) * D + lane * C::DPL + e] = acc[h][e];
+        for (int e = 0; e < C::DPL / 2; ++e)
+            reinterpret_cast<float2*>(accw + (warp * G + h) * D + lane * C::DPL)[e] = acc[h][e];
     named_barrier_sync(1, NCW * 32);
     for (int idx = threadIdx.x; idx < G * D; idx += NCW * 32) {
         const int h = idx / D, d = idx % D;

@@ -7,9 +7,11 @@
 // under which split attention equals single-pass attention.  Partitions with
 // l_p = 0 (no visible token for that row) carry no weight.
 //
-// One warp per (row, head): lanes take 32 partitions at a time, compute their
-// weights, and broadcast them by shuffle while every lane accumulates its
-// head_dim/32 output dims (coalesced 128-bit or 64-bit loads of o_p).
+// One CTA of 256 threads per (row, head): the partitions' (m_p, l_p) are read
+// in parallel and reduced to M and the weights w_p in shared memory; then
+// thread (group k, chunk c) accumulates w_p * o_p over partitions p = k, k+8,
+// ... for its 16-byte chunk of head_dim, with four independent loads in
+// flight; the eight groups are summed through shared memory.
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -17,64 +19,103 @@ namespace pkv {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kThreads = 256;
+constexpr int kMaxStaged = 2048;   // partitions whose weights fit the shared buffer at once
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(ReduceParams p) {
-    constexpr int DPL = D / 32;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int r = blockIdx.x;
+__global__ void __launch_bounds__(kThreads) lse_reduce_kernel(ReduceParams p) {
+    constexpr int CH = D / 4;              // float4 chunks of one row
+    constexpr int NGRP = kThreads / CH;    // partition groups (8 for D=128, 16 for D=64)
+    __shared__ float w_s[kMaxStaged];
+    __shared__ float red[kThreads / 32];
+    __shared__ float4 part[kThreads];
+    const int r = blockIdx.x, h = blockIdx.y;
     const int s = r / p.q_len;
     int ctx = p.context_lens[s];
     if (ctx < 0) ctx = 0;
     int nparts = (ctx + p.partition_size - 1) / p.partition_size;
     if (nparts > p.max_partitions) nparts = p.max_partitions;
-    for (int h = blockIdx.y * kWarps + warp; h < p.num_heads; h += gridDim.y * kWarps) {
-        const size_t base = (size_t(r) * p.num_heads + h) * p.max_partitions;
-        // pass 1: global max over partitions with weight
-        float M = -INFINITY;
-        for (int i = lane; i < nparts; i += 32)
-            if (p.exp_sums[base + i] > 0.f) M = fmaxf(M, p.max_logits[base + i]);
+    const size_t base = (size_t(r) * p.num_heads + h) * p.max_partitions;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    // M = max over partitions with weight
+    float M = -INFINITY;
+    for (int i = tid; i < nparts; i += kThreads)
+        if (p.exp_sums[base + i] > 0.f) M = fmaxf(M, p.max_logits[base + i]);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float acc[DPL];
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    if (lane == 0) red[warp] = M;
+    __syncthreads();
+    M = red[0];
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-        float W = 0.f;
-        if (M != -INFINITY) {
-            for (int c0 = 0; c0 < nparts; c0 += 32) {
-                const int i = c0 + lane;
-                float w = 0.f;
-                if (i < nparts) {
-                    const float l = p.exp_sums[base + i];
-                    if (l > 0.f) w = l * exp2f((p.max_logits[base + i] - M) * kLog2e);
-                }
+    for (int w = 1; w < kThreads / 32; ++w) M = fmaxf(M, red[w]);
+    __syncthreads();
+
+    const int grp = tid / CH, c = tid % CH;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    if (M != -INFINITY) {
+        for (int p0 = 0; p0 < nparts; p0 += kMaxStaged) {
+            const int n = min(kMaxStaged, nparts - p0);
+            for (int i = tid; i < n; i += kThreads) {
+                const float l = p.exp_sums[base + p0 + i];
+                const float w = (l > 0.f) ? l * exp2f((p.max_logits[base + p0 + i] - M) * kLog2e) : 0.f;
+                w_s[i] = w;
                 W += w;
-                const int n = min(32, nparts - c0);
-                for (int k = 0; k < n; ++k) {
-                    const float wk = __shfl_sync(0xffffffffu, w, k);
-                    if (wk == 0.f) continue;
-                    const float* o = p.tmp_out + (base + c0 + k) * D + lane * DPL;
-                    if constexpr (DPL == 4) {
-                        const float4 v = *reinterpret_cast<const float4*>(o);
-                        acc[0] = fmaf(wk, v.x, acc[0]);
-                        acc[1] = fmaf(wk, v.y, acc[1]);
-                        acc[2] = fmaf(wk, v.z, acc[2]);
-                        acc[3] = fmaf(wk, v.w, acc[3]);
-                    } else {
-                        const float2 v = *reinterpret_cast<const float2*>(o);
-                        acc[0] = fmaf(wk, v.x, acc[0]);
-                        acc[1] = fmaf(wk, v.y, acc[1]);
+            }
+            __syncthreads();
+            int i = grp;
+            for (; i + 3 * NGRP < n; i += 4 * NGRP) {   // four independent loads in flight
+                float4 v[4];
+                float wk[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    wk[u] = w_s[i + u * NGRP];
+                    v[u] = *reinterpret_cast<const float4*>(p.tmp_out + (base + p0 + i + u * NGRP) * D + 4 * c);
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (wk[u] != 0.f) {
+                        acc.x = fmaf(wk[u], v[u].x, acc.x);
+                        acc.y = fmaf(wk[u], v[u].y, acc.y);
+                        acc.z = fmaf(wk[u], v[u].z, acc.z);
+                        acc.w = fmaf(wk[u], v[u].w, acc.w);
                     }
+            }
+            for (; i < n; i += NGRP) {
+                const float wk = w_s[i];
+                if (wk != 0.f) {
+                    const float4 v = *reinterpret_cast<const float4*>(p.tmp_out + (base + p0 + i) * D + 4 * c);
+                    acc.x = fmaf(wk, v.x, acc.x);
+                    acc.y = fmaf(wk, v.y, acc.y);
+                    acc.z = fmaf(wk, v.z, acc.z);
+                    acc.w = fmaf(wk, v.w, acc.w);
                 }
             }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+            __syncthreads();
         }
-        const float inv = (W > 0.f) ? 1.f / W : 0.f;
-        const size_t ob = (size_t(r) * p.num_heads + h) * D + lane * DPL;
+    }
+    // W: block sum of the weights
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) store_out(p.out, p.out_dtype, ob + e, acc[e] * inv);
+    for (int o = 16; o >= 1; o >>= 1) W += __shfl_xor_sync(0xffffffffu, W, o);
+    if (lane == 0) red[warp] = W;
+    part[tid] = acc;
+    __syncthreads();
+    if (tid < CH) {
+        float Wt = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) Wt += red[w];
+        float4 o = part[tid];
+        for (int k = 1; k < NGRP; ++k) {
+            const float4 v = part[k * CH + tid];
+            o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
+        }
+        const float inv = (Wt > 0.f) ? 1.f / Wt : 0.f;
+        const size_t ob = (size_t(r) * p.num_heads + h) * D + 4 * tid;
+        store_out(p.out, p.out_dtype, ob + 0, o.x * inv);
+        store_out(p.out, p.out_dtype, ob + 1, o.y * inv);
+        store_out(p.out, p.out_dtype, ob + 2, o.z * inv);
+        store_out(p.out, p.out_dtype, ob + 3, o.w * inv);
     }
 }
 
@@ -82,13 +123,12 @@ __global__ void __launch_bounds__(kWarps * 32) lse_reduce_kernel(ReduceParams p)
 
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream) {
     const int rows = p.num_seqs * p.q_len;
-    int hy = (p.num_heads + kWarps - 1) / kWarps;
-    if (hy > 65535) hy = 65535;
-    dim3 grid(rows, hy);
+    if (p.num_heads > 65535) return cudaErrorInvalidValue;
+    dim3 grid(rows, p.num_heads);
     if (p.head_dim == 128)
-        lse_reduce_kernel<128><<<grid, kWarps * 32, 0, stream>>>(p);
+        lse_reduce_kernel<128><<<grid, kThreads, 0, stream>>>(p);
     else
-        lse_reduce_kernel<64><<<grid, kWarps * 32, 0, stream>>>(p);
+        lse_reduce_kernel<64><<<grid, kThreads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -1,0 +1,119 @@
+"""GPU parity of the tensor-core kernel: multi-token verify blocks on fp16/bf16
+caches and the K8/V4 quantised cache, against the oracle (which dequantises
+the same codes and scales exactly).
+
+Tolerances: verify rows as for single-query decode (fp32 accumulation of
+bf16/fp16 products); K8/V4 max-abs 2e-2 against the identically-dequantised
+oracle (the kernel rounds q and p*scale_v to fp16 for the MMA)."""
+import numpy as np
+import pytest
+import torch
+
+from paged_decode_attention_cache_gb300 import ops, workloads as W
+from paged_decode_attention_cache_gb300.runner import DecodeStep
+from tests.helpers import bits, oracle_attention, oracle_cache_after_step
+from tests.test_gpu_parity import check_attention
+
+pytestmark = pytest.mark.gpu
+
+K8V4_ABS = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from paged_decode_attention_cache_gb300 import build
+    build.build()
+    ops.lib()
+    torch.cuda.set_device(0)
+
+
+def run(w, part, out_dtype=torch.float32):
+    st = DecodeStep(w, "cuda", partition_size=part, out_dtype=out_dtype)
+    out = st.step()
+    torch.cuda.synchronize()
+    assert st.error_flags() == 0, f"device error flags {st.error_flags():#x}"
+    return st, out.double().cpu().numpy()
+
+
+# ---------------------------------------------------------------- verify (q_len > 1)
+
+VERIFY = []
+for D in (64, 128):
+    for H, Hkv, ql in ((8, 2, 4), (32, 8, 4), (4, 4, 16), (16, 2, 2), (8, 8, 3), (16, 2, 1)):
+        VERIFY.append((D, H, Hkv, ql))
+
+
+@pytest.mark.parametrize("D,H,Hkv,ql", VERIFY)
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("part", [0, 32, 512])
+def test_verify_small(D, H, Hkv, ql, dt, part):
+    if ql == 1 and part == 512:
+        pytest.skip("q_len 1 on fp16/bf16 runs the CUDA-core kernel")
+    ctx = [2, 3, 4, 5, 16, 17, 100, 513]
+    w = W.build(name="t", seed=200 + D + H + ql, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
+                cache=dt, q_len=ql)
+    ref = oracle_attention(w, threads=8)
+    _, got = run(w, part)
+    check_attention(got, ref, False)
+
+
+def test_verify_batch256_full_sampled_rows():
+    w = W.verify_batch256(device="cuda")
+    st, got = run(w, 512)
+    cs = oracle_cache_after_step(w)
+    # the drafts' K/V were written by the step: whole pool bit-exact
+    assert np.array_equal(bits(st.cache.k), cs["k"]) and np.array_equal(bits(st.cache.v), cs["v"])
+    rng = np.random.default_rng(0)
+    seqs = np.concatenate([[int(np.argmax(w.context_lens.cpu())), int(np.argmin(w.context_lens.cpu()))],
+                           rng.choice(w.num_seqs, 14, replace=False)])
+    rows = sorted({int(s) * 4 + j for s in seqs for j in range(4)})
+    ref = oracle_attention(w, cs, rows=rows, threads=16)
+    check_attention(got[rows], ref[rows], False)
+    _, got16 = run(w, 512, torch.bfloat16)
+    check_attention(got16[rows], ref[rows], True)
+
+
+# ---------------------------------------------------------------- K8/V4
+
+K8 = []
+for D in (64, 128):
+    for H, Hkv, ql in ((8, 2, 1), (32, 8, 1), (4, 4, 1), (16, 2, 1), (8, 2, 4)):
+        K8.append((D, H, Hkv, ql))
+
+
+@pytest.mark.parametrize("D,H,Hkv,ql", K8)
+@pytest.mark.parametrize("part", [0, 48, 512])
+def test_k8v4_small(D, H, Hkv, ql, part):
+    ctx = [1, 5, 16, 17, 100, 511, 513] if ql == 1 else [4, 5, 17, 100, 513]
+    w = W.build(name="t", seed=300 + D + H + ql, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
+                cache="k8v4", q_len=ql)
+    cs = oracle_cache_after_step(w)
+    ref = oracle_attention(w, cs, threads=8)
+    st, got = run(w, part)
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= K8V4_ABS, f"max abs err {err:.3e}"
+    # the codes the kernel read are the oracle's codes
+    qc = cs["qc"]
+    assert np.array_equal(st.cache.k.cpu().numpy(), qc.k_q)
+    assert np.array_equal(bits(st.cache.v_scale), qc.v_scale)
+
+
+def test_k8v4_fp16_queries():
+    w = W.build(name="t", seed=77, context_lens=[300, 40], num_heads=32, num_kv_heads=8, head_dim=128,
+                cache="k8v4", src_dtype="f16")
+    ref = oracle_attention(w, threads=8)
+    _, got = run(w, 128)
+    assert np.abs(got - ref).max() <= K8V4_ABS
+
+
+def test_k8v4_batch32_full_sampled_rows():
+    w = W.k8v4_batch32(device="cuda")
+    st, got = run(w, 512)
+    cs = oracle_cache_after_step(w)
+    rows = sorted(set([0, 31, int(np.argmax(w.context_lens.cpu()))] + list(range(3, 32, 5))))
+    ref = oracle_attention(w, cs, rows=rows, threads=16)
+    err = np.abs(got[rows] - ref[rows]).max()
+    assert err <= K8V4_ABS, f"max abs err {err:.3e}"
+    _, got1 = run(w, 0)
+    assert np.abs(got1[rows] - ref[rows]).max() <= K8V4_ABS
