@@ -41,6 +41,13 @@ WORKLOADS = {
     "verify_batch256": 5,
 }
 DEFAULT_WORKLOAD = "llama3_8b_batch8"
+# schedule of the attention call per workload: the 32K workload is defined with
+# fixed 512-token partitions and a separate reduce; the batched ones use the
+# balanced split with its fused combine; the tiny one is a single pass
+DEFAULT_SCHEDULE = {"tiny_f16": "single", "llama3_8b_batch8": "balanced", "long_context_32k": "split",
+                    "k8v4_batch32": "balanced", "verify_batch256": "balanced"}
+KERNEL_NAME = {"single": "pkv_paged_attention", "split": "pkv_paged_attention_split",
+               "balanced": "pkv_paged_attention_balanced"}
 
 
 def parse():
@@ -49,7 +56,9 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--partition", type=int, default=None, help="split-KV partition size (0 = single pass)")
+    ap.add_argument("--partition", type=int, default=None, help="split-KV partition size (with --schedule split)")
+    ap.add_argument("--schedule", default=None, choices=["single", "split", "balanced"],
+                    help="attention schedule (default: per workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -174,7 +183,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, attn_bytes, budget_s):
+def cpu_baseline(w, attn_bytes, budget_s, split=False):
     """The oracle as it stands, on this host's cores, over whole steps of the
     same workload until the time budget is spent (at least one step)."""
     import numpy as np  # noqa: F401
@@ -182,7 +191,7 @@ def cpu_baseline(w, attn_bytes, budget_s):
     threads = os.cpu_count() or 1
     cs = oracle_cache_after_step(w)
     import oracle
-    split = w.partition_size > 0
+    split = split and w.partition_size > 0
     n, t0 = 0, time.perf_counter()
     while True:
         if split:   # phase 1 partials, then the LSE reduce, as the GPU step does
@@ -207,7 +216,8 @@ def run_reference(args):
         return 0
     w = make_workload(args.workload, "cpu", 0, args.partition)
     attn_b, wr_b = step_bytes(w)
-    cb = cpu_baseline(w, attn_b + wr_b, max(1.0, min(args.cpu_seconds, 20.0)))
+    schedule = args.schedule or DEFAULT_SCHEDULE[args.workload]
+    cb = cpu_baseline(w, attn_b + wr_b, max(1.0, min(args.cpu_seconds, 20.0)), split=(schedule == "split"))
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds_per_step"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -243,7 +253,12 @@ def main():
     l2 = getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_BYTES_FALLBACK
     reps = max(2, math.ceil(3 * l2 / max(1, total_b)))
     reps = min(reps, 16)
-    steps_ = [DecodeStep(w, dev) for _ in range(reps)]
+    schedule = args.schedule or DEFAULT_SCHEDULE[args.workload]
+    if args.partition is not None and args.schedule is None:
+        schedule = "split" if args.partition > 0 else "single"
+    if schedule == "split" and w.partition_size <= 0:
+        w.partition_size = 512
+    steps_ = [DecodeStep(w, dev, schedule=schedule) for _ in range(reps)]
     launches = steps_[0].launches_per_step()
 
     for i in range(max(3, args.warmup)):
@@ -350,7 +365,7 @@ def main():
 
     peak, peak_src = load_peaks()
     achieved = attn_b / (kern_ms * 1e-3) / 1e9
-    kernel_name = "paged_attention_split" if steps_[0].split else "paged_attention"
+    kernel_name = KERNEL_NAME[schedule]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic_from_profiles(w.name, kernel_name), "kernel": kernel_name,
                 "kernel_ms": kern_ms, "peak_source": f"{peak_src} (copy bandwidth)",
@@ -358,7 +373,7 @@ def main():
     cb = None
     if rank == 0 and not (args.no_cpu_baseline or args.quick):
         wc = make_workload(args.workload, "cpu", 0, args.partition)
-        cb = cpu_baseline(wc, total_b, args.cpu_seconds)
+        cb = cpu_baseline(wc, total_b, args.cpu_seconds, split=(schedule == "split"))
         cb.pop("seconds_per_step", None)
 
     if ws > 1:
@@ -372,7 +387,8 @@ def main():
         "dtype": "f32", "data": "synthetic",
         "config": {"workload": w.name, "batch": w.num_seqs, "q_len": w.q_len, "heads": w.num_heads,
                    "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "cache": w.cache,
-                   "partition_size": steps_[0].partition_size, "sum_context": int(w.context_lens.sum()),
+                   "schedule": schedule, "partition_size": steps_[0].partition_size,
+                   "sum_context": int(w.context_lens.sum()),
                    "bytes_per_step": total_b, "parallelism": f"replicas x{ws}",
                    "l2": f"{reps} rotating input replicas, {reps * total_b / 2**20:.0f} MiB touched per cycle "
                          f"vs {l2 / 2**20:.0f} MiB L2"},

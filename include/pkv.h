@@ -165,9 +165,9 @@ pkv_status pkv_quantize_kv(const pkv_cache *cache, const void *k_new, const void
  *   scale  multiplies q.k before the softmax (usually 1/sqrt(head_dim)).
  * out[r, h] = sum_t softmax_t(scale * q[r,h] . K[t, h/g]) V[t, h/g] over the
  * visible tokens of row r; a row with no visible token gets zeros.
- * One CTA per (sequence, kv head) serves all g query heads of the group, so
- * each KV block is read from HBM once per step.  q_len > 1 requires
- * g * q_len <= 16 and an fp16/bf16 cache.
+ * Each (sequence, kv head) is handled whole by one CTA, which serves all g
+ * query heads of the group, so each KV block is read from HBM once per step.
+ * q_len > 1 (and the K8V4 cache) requires g * q_len <= 16.
  */
 pkv_status pkv_paged_attention(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
                                int32_t num_heads, float scale, const pkv_cache *cache,
@@ -217,6 +217,36 @@ pkv_status pkv_reduce(void *out, pkv_dtype out_dtype, const float *tmp_out,
                       const float *max_logits, const float *exp_sums, const pkv_seqs *seqs,
                       int32_t num_heads, int32_t head_dim, int32_t partition_size,
                       int32_t max_partitions, pkv_stream_t stream);
+
+/*
+ * Bytes of scratch for pkv_paged_attention_balanced: per-piece partial outputs
+ * and max/sum pairs for up to 1024 CTAs plus one piece per (sequence, kv
+ * head), and one int32 counter per (sequence, kv head).  Returns 0 for
+ * non-positive arguments.
+ */
+size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim);
+
+/*
+ * Paged attention with split-KV partitions chosen for balance, in one launch
+ * [mlxcel manual "KV Cache", §"Paged Decode Storage and Kernels": decode
+ * splits; METAL: split-KV decode kernels].  Same result and arguments as
+ * pkv_paged_attention; the difference is the schedule: one persistent CTA per
+ * SM, and the batch's (sequence, kv head, 16-token block) list cut into equal
+ * contiguous ranges, so a long sequence is spread over many SMs and a short one
+ * shares an SM with its neighbours.  A (sequence, kv head) cut into pieces
+ * leaves one partial per piece in `workspace`; the CTA that finishes its last
+ * piece combines them with the log-sum-exp identity of pkv_reduce (an atomic
+ * count decides who, nobody waits).
+ *   workspace  device memory of pkv_balanced_workspace_bytes() bytes, 256-byte
+ *              aligned, ZERO-FILLED before its first use; every call leaves its
+ *              counters at zero again, so it can be reused without clearing
+ *              (clear it again after a call that reported a device error).
+ *              Calls that share one workspace must not overlap on the GPU.
+ */
+pkv_status pkv_paged_attention_balanced(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                        int32_t num_heads, float scale, const pkv_cache *cache,
+                                        const pkv_seqs *seqs, void *workspace, size_t workspace_bytes,
+                                        uint32_t *err_flags, pkv_stream_t stream);
 
 /*
  * Copy every visible token of every sequence back to contiguous storage

@@ -158,9 +158,7 @@ pkv_status attn_setup(pkv::AttnParams* p, const void* q, pkv_dtype q_dtype, int3
     if (*gqa != 1 && *gqa != 2 && *gqa != 4 && *gqa != 8)
         return fail(PKV_ERR_UNSUPPORTED, "group size %d (1, 2, 4 or 8)", *gqa);
     if (!(scale == scale)) return fail(PKV_ERR_INVALID_ARG, "scale is NaN");
-    const bool tc = seqs->q_len > 1 || cache->kind == PKV_CACHE_K8V4;
-    if (tc ? !pkv::decode_tc_supported(cache->kind, cache->head_dim, *gqa, seqs->q_len)
-           : !pkv::decode_cc_supported(cache->kind, cache->head_dim, *gqa))
+    if (!pkv::attention_supported(cache->kind, cache->head_dim, *gqa, seqs->q_len))
         return fail(PKV_ERR_UNSUPPORTED, "no kernel for cache kind %d, head_dim %d, group %d, q_len %d", cache->kind,
                     cache->head_dim, *gqa, seqs->q_len);
     *p = pkv::AttnParams{};
@@ -183,16 +181,13 @@ pkv_status attn_setup(pkv::AttnParams* p, const void* q, pkv_dtype q_dtype, int3
     return PKV_OK;
 }
 
-pkv_status attn_launch(const pkv::AttnParams& p, const pkv_cache* cache, int gqa, int grid_parts,
-                       pkv_stream_t stream) {
-    const bool tc = p.q_len > 1 || cache->kind == PKV_CACHE_K8V4;
+pkv_status attn_launch(pkv::AttnParams p, const pkv_cache* cache, int gqa, pkv_stream_t stream) {
+    const bool tc = pkv::attention_uses_tensor_cores(cache->kind, p.q_len);
     CUtensorMap km, vm;
     pkv_status st = cache_maps(cache, &km, &vm, tc);
     if (st != PKV_OK) return st;
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = tc ? pkv::launch_decode_tc(p, cache->kind, gqa, km, vm, grid_parts, s)
-                       : pkv::launch_decode_cc(p, cache->kind, gqa, km, vm, grid_parts, s);
-    return cuda_result(e, "attention launch");
+    return cuda_result(pkv::launch_attention(p, cache->kind, gqa, km, vm, reinterpret_cast<cudaStream_t>(stream)),
+                       "attention launch");
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -271,7 +266,8 @@ pkv_status pkv_paged_attention(void* out, pkv_dtype out_dtype, const void* q, pk
     p.out_dtype = out_dtype;
     p.partition_blocks = seqs->max_blocks_per_seq;
     p.max_partitions = 1;
-    return attn_launch(p, cache, gqa, 1, stream);
+    p.mode = pkv::kModeSingle;
+    return attn_launch(p, cache, gqa, stream);
 }
 
 size_t pkv_split_workspace_bytes(int32_t num_rows, int32_t num_heads, int32_t head_dim, int32_t max_partitions) {
@@ -304,8 +300,48 @@ pkv_status pkv_paged_attention_split(float* tmp_out, float* max_logits, float* e
     p.exp_sums = exp_sums;
     p.partition_blocks = partition_size / 16;
     p.max_partitions = max_partitions;
-    const int grid_parts = int((int64_t(seqs->max_blocks_per_seq) * 16 + partition_size - 1) / partition_size);
-    return attn_launch(p, cache, gqa, grid_parts, stream);
+    p.mode = pkv::kModeSplit;
+    return attn_launch(p, cache, gqa, stream);
+}
+
+size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim) {
+    if (num_seqs <= 0 || num_kv_heads <= 0 || head_dim <= 0) return 0;
+    return pkv::balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim);
+}
+
+pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
+                                        int32_t num_heads, float scale, const pkv_cache* cache, const pkv_seqs* seqs,
+                                        void* workspace, size_t workspace_bytes, uint32_t* err_flags,
+                                        pkv_stream_t stream) {
+    pkv::AttnParams p;
+    int gqa = 0;
+    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
+    if (st != PKV_OK) return st;
+    CHECK_PTR(out, "out");
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+        return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (seqs->num_seqs == 0) return ok();
+    const size_t need = pkv::balanced_workspace_bytes(seqs->num_seqs, cache->num_kv_heads, cache->head_dim);
+    if (!workspace) return fail(PKV_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(PKV_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+    if (workspace_bytes < need)
+        return fail(PKV_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    const size_t pairs = size_t(seqs->num_seqs) * size_t(cache->num_kv_heads);
+    const size_t slots = size_t(pkv::kMaxGrid) + pairs;
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    p.part_o = reinterpret_cast<float*>(w);
+    w += align256(slots * 16 * size_t(cache->head_dim) * 4);
+    p.part_ml = reinterpret_cast<float*>(w);
+    w += align256(slots * 16 * 2 * 4);
+    p.counters = reinterpret_cast<int32_t*>(w);
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.partition_blocks = seqs->max_blocks_per_seq;
+    p.max_partitions = 1;
+    p.mode = pkv::kModeBalanced;
+    p.min_chunk = 8;
+    return attn_launch(p, cache, gqa, stream);
 }
 
 pkv_status pkv_reduce(void* out, pkv_dtype out_dtype, const float* tmp_out, const float* max_logits,

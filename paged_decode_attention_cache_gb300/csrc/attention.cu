@@ -1,0 +1,1105 @@
+// attention.cu -- persistent paged attention: one CTA per SM, a deep TMA ring,
+// and the whole batch's work list split into contiguous per-CTA ranges.
+//
+// What it computes [metalworking "The KV Cache": the pagedattention kernel,
+// GQA as the stride trick kv_head = q_head / gqa_factor, split-KV decode;
+// MTPLX "How MTPLX Manages Memory Using Request-Sized Paged KV Cache",
+// §"Kernel Interface and Memory Slicing": only the stored tokens are read;
+// mlxcel manual "KV Cache", §"Speculative Rewind": a verify block of q_len
+// drafts, draft j seeing the history and drafts 0..j]:
+//   out[r, h] = sum_t softmax_t(scale * q[r,h] . K[t, h/g]) V[t, h/g]
+//
+// Work list.  The units of the batch are laid out sequence by sequence, kv head
+// by kv head, and CTA c takes units [c*chunk, (c+1)*chunk):
+//   single pass  unit = one (sequence, kv head) pair -> final output;
+//   split        unit = one partition of partition_size tokens of a pair ->
+//                normalised partial (o_p, m_p, l_p) for the LSE reduce;
+//   balanced     unit = one 16-token block of a pair, chunk = ceil(blocks/grid):
+//                every CTA streams the same number of blocks; a pair cut between
+//                CTAs leaves one unnormalised partial per piece in the
+//                workspace, and the CTA that finishes its pair's last piece
+//                (an atomic count, no waiting) combines the pieces by the same
+//                log-sum-exp identity and writes the output.
+//
+// CTA anatomy (256 threads).  Warp 7 produces: for each 16-token block it reads
+// the block table (32 entries per load), waits for a free ring stage and issues
+// the TMA tile loads (and, for the K8/V4 cache, 1-D bulk copies of the block's
+// scales and zeros).  Warps 0-6 consume whole blocks round-robin, each with its
+// own online-softmax state (running max m, sum l, unnormalised accumulator),
+// and merge through shared memory at the end of every segment (the part of a
+// pair that this CTA owns) while the producer already streams the next one.
+// The ring holds `stages` blocks (≈190 KB), so one SM keeps tens of KB of HBM
+// reads in flight however long its consumers spend on a block.
+//
+// Two block-math policies:
+//   CcMath  fp16/bf16 cache, q_len 1, CUDA cores: q in registers as fp32 pairs,
+//           8 or 16 lanes per token with packed fma.rn.f32x2, reduce-scatter
+//           shuffles, softmax over the block's 16 x g scores in shared memory,
+//           PV with head_dim/32 dims per lane;
+//   TcMath  verify blocks (q_len > 1) and the K8/V4 cache, tensor cores
+//           (mma.sync m16n8k16, fp32 accumulate) on 16 query rows (g heads x
+//           q_len drafts), TMA-swizzled tiles read by ldmatrix; int8/int4 codes
+//           become exact fp16 integers in registers, the K scale multiplies the
+//           scores, the V scale multiplies P per group, the V zero-point term is
+//           summed on CUDA cores.
+// Every mbarrier wait is bounded; a wait that gives up flags
+// PKV_DEVERR_TIMEOUT and the block is skipped.
+#include "pkv_device.cuh"
+#include "pkv_internal.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kBS = 16;
+constexpr int kNCW = 7;                       // consumer warps (8 warps in all: one SM sub-partition
+                                              // then holds two, so a thread may use up to 255 registers)
+constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kMaxRows = 16;                  // query rows per (sequence, kv head)
+constexpr int kSmemLimit = 227 * 1024;
+
+constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- small device helpers
+
+template <int W>
+__device__ __forceinline__ int swz(int c, int t) {   // 16-byte chunk c of row t under the W-byte TMA swizzle
+    return c ^ ((t * W >> 7) & (W / 16 - 1));
+}
+
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <bool BF>
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (BF)
+        mma_bf16(d, a, b0, b1);
+    else
+        mma_f16(d, a, b0, b1);
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// Four int8 codes (code e in byte e) -> two fp16x2 of the exact integers: flip
+// the sign bit (c + 128 in 0..255), splice each byte under the fp16 exponent
+// of 1024 (0x64xx = 1024 + byte), subtract 1152.
+__device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    const uint32_t a = __byte_perm(x, 0x64646464u, 0x5140);
+    const uint32_t b = __byte_perm(x, 0x64646464u, 0x7362);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
+    lo = *reinterpret_cast<uint32_t*>(&ha);
+    hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// Nibble i of both 16-bit halves of w -> fp16x2 of the exact integers 0..15.
+__device__ __forceinline__ uint32_t u4pair_to_f16x2(uint32_t w, int i) {
+    const uint32_t x = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;   // 1024 + code
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6400), __ushort_as_half(0x6400));
+    __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&x), bias);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <int N>
+__device__ __forceinline__ void load_f(const float* src, float (&v)[N]) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + i);
+            v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+        }
+    } else if constexpr (N == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        v[0] = x.x; v[1] = x.y;
+    } else {
+        v[0] = src[0];
+    }
+}
+
+template <int N>
+__device__ __forceinline__ void load_f2(const float2* src, float2 (&v)[N]) {
+    if constexpr (N >= 2) {
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            const float4 x = *reinterpret_cast<const float4*>(src + i);
+            v[i] = make_float2(x.x, x.y);
+            v[i + 1] = make_float2(x.z, x.w);
+        }
+    } else {
+        v[0] = src[0];
+    }
+}
+
+// ---------------------------------------------------------------- CUDA-core block math
+
+template <typename T, int D, int G>
+struct CcMath {
+    static constexpr bool kTensor = false;
+    static constexpr int CH = D / 8;                               // 16-byte chunks per row
+    static constexpr int LPT = (G * D / 64 > 8) ? G * D / 64 : 8;  // lanes per token (QK)
+    static constexpr int TPP = 32 / LPT;                           // tokens per pass
+    static constexpr int NPASS = kBS / TPP;
+    static constexpr int CPL = CH / LPT;                           // chunks per lane
+    static constexpr int DPL = D / 32;                             // dims per lane (PV)
+    static constexpr int KT = kBS * D * 2;                         // K (or V) tile bytes
+    static constexpr int TX = 2 * KT;                              // bytes landing per stage
+    static constexpr int STAGE = 2 * KT;
+    static constexpr int SCRATCH = align_up(kBS * G * 4 + kBS * G * 8 + G * 4, 16);   // per warp
+    static_assert(CPL >= 1 && CH % LPT == 0, "bad lane split");
+
+    float2 q2[G][CPL * 4];
+    float m_run, l_run;            // for head lane % G
+    float2 acc[G][DPL / 2];
+    int my_head;
+    bool writer;
+
+    static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
+                                                 const AttnParams&, int kvh, int pb, uint64_t* bar) {
+        // byte-addressed maps, box = one kv head's 16 rows
+        tma_load_2d(dst, km, kvh * D * 2, pb * kBS, bar);
+        tma_load_2d(dst + KT, vm, kvh * D * 2, pb * kBS, bar);
+    }
+
+    __device__ __forceinline__ void init(int lane) {
+        const int jl = lane % LPT;
+        my_head = 0;
+#pragma unroll
+        for (int o = LPT / 2, nv = G; nv > 1; o >>= 1, nv >>= 1)
+            if (jl & o) my_head += nv / 2;
+        writer = (jl & (LPT / G - 1)) == 0;
+    }
+
+    __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int /*ctx*/, int lane) {
+        const int jl = lane % LPT;
+        const T* qrow = reinterpret_cast<const T*>(p.q) + (size_t(s) * p.num_heads + kvh * G) * D;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(qrow + h * D + (jl + k * LPT) * 8);
+                const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = Half16<T>::unpack2(wds[i]);
+                    q2[h][k * 4 + i] = make_float2(f.x * p.scale_log2, f.y * p.scale_log2);
+                }
+            }
+        m_run = -INFINITY;
+        l_run = 0.f;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < DPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
+    }
+
+    __device__ __forceinline__ void block(const uint8_t* stg, int /*pos0*/, int ntok, uint8_t* scratch, int lane) {
+        float* sc = reinterpret_cast<float*>(scratch);
+        float2* pc = reinterpret_cast<float2*>(scratch + kBS * G * 4);
+        float* alph = reinterpret_cast<float*>(scratch + kBS * G * 12);
+        const int grp = lane / LPT, jl = lane % LPT;
+        const T* Ks = reinterpret_cast<const T*>(stg);
+        const T* Vs = Ks + kBS * D;
+        // ---- scores: sc[t*G + h] = log2e * scale * q_h . k_t
+#pragma unroll
+        for (int pass = 0; pass < NPASS; ++pass) {
+            const int t = pass * TPP + grp;
+            float2 a2[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) a2[h] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                const uint4 raw = *reinterpret_cast<const uint4*>(Ks + t * D + (jl + k * LPT) * 8);
+                const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = Half16<T>::unpack2(wds[i]);
+#pragma unroll
+                    for (int h = 0; h < G; ++h) a2[h] = __ffma2_rn(q2[h][k * 4 + i], f, a2[h]);
+                }
+            }
+            float a[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) a[h] = a2[h].x + a2[h].y;
+            // reduce-scatter over the token's LPT lanes: halve the live heads per level
+#pragma unroll
+            for (int o = LPT / 2, nv = G; o >= 1; o >>= 1) {
+                const bool up = (jl & o) != 0;
+                if (nv > 1) {
+#pragma unroll
+                    for (int i = 0; i < nv / 2; ++i) {
+                        const float send = up ? a[i] : a[i + nv / 2];
+                        const float keep = up ? a[i + nv / 2] : a[i];
+                        a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                    }
+                    nv >>= 1;
+                } else {
+                    a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
+                }
+            }
+            if (writer) sc[t * G + my_head] = (t < ntok) ? a[0] : -INFINITY;
+        }
+        __syncwarp();
+        // ---- online softmax over the block's 16 x G scores
+        constexpr int NE = kBS * G;
+        constexpr int EPL = (NE + 31) / 32;
+        float x[EPL];
+        float bm = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            x[i] = (e < NE) ? sc[e] : -INFINITY;
+            bm = fmaxf(bm, x[i]);
+        }
+#pragma unroll
+        for (int o = G; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+        const float m_new = fmaxf(m_run, bm);
+        float bsum = 0.f;
+#pragma unroll
+        for (int i = 0; i < EPL; ++i) {
+            const int e = lane + 32 * i;
+            const float pe = exp2f(x[i] - m_new);
+            bsum += pe;
+            if (e < NE) pc[e] = make_float2(pe, pe);
+        }
+#pragma unroll
+        for (int o = G; o < 32; o <<= 1) bsum += __shfl_xor_sync(0xffffffffu, bsum, o);
+        const float al = exp2f(m_run - m_new);
+        l_run = l_run * al + bsum;
+        m_run = m_new;
+        if (lane < G) alph[lane] = al;
+        __syncwarp();
+        // ---- acc = acc * alpha + sum_t p_t V_t
+        {
+            float alv[G];
+            load_f<G>(alph, alv);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) acc[h][e] = __fmul2_rn(acc[h][e], make_float2(alv[h], alv[h]));
+        }
+        auto pv_token = [&](int t) {
+            float2 vf[DPL / 2];
+            if constexpr (DPL == 4) {
+                const uint2 raw = *reinterpret_cast<const uint2*>(Vs + t * D + lane * 4);
+                vf[0] = Half16<T>::unpack2(raw.x);
+                vf[1] = Half16<T>::unpack2(raw.y);
+            } else {
+                vf[0] = Half16<T>::unpack2(*reinterpret_cast<const uint32_t*>(Vs + t * D + lane * 2));
+            }
+            float2 pp[G];
+            load_f2<G>(pc + t * G, pp);
+#pragma unroll
+            for (int h = 0; h < G; ++h)
+#pragma unroll
+                for (int e = 0; e < DPL / 2; ++e) acc[h][e] = __ffma2_rn(pp[h], vf[e], acc[h][e]);
+        };
+        if (ntok == kBS) {
+#pragma unroll
+            for (int t = 0; t < kBS; ++t) pv_token(t);
+        } else {
+#pragma unroll 1
+            for (int t = 0; t < ntok; ++t) pv_token(t);
+        }
+        __syncwarp();
+    }
+
+    __device__ __forceinline__ void finish(int) {}
+
+    // unnormalised accumulator rows [G][D] and per-row (m, l) of this warp
+    __device__ __forceinline__ void store(float* ob, float* mw, float* lw, int /*M*/, int lane) const {
+        if (lane < G) {
+            mw[lane] = m_run;
+            lw[lane] = l_run;
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+#pragma unroll
+            for (int e = 0; e < DPL / 2; ++e) reinterpret_cast<float2*>(ob + h * D + lane * DPL)[e] = acc[h][e];
+    }
+};
+
+// ---------------------------------------------------------------- tensor-core block math
+
+template <int KIND, int D>
+struct TcMath {
+    static constexpr bool kTensor = true;
+    static constexpr bool Q8 = KIND == PKV_CACHE_K8V4;
+    static constexpr bool BF = KIND == PKV_CACHE_BF16;
+    static constexpr int NG = D / 32;
+    static constexpr int NKS = D / 16;
+    static constexpr int NNT = D / 8;
+    static constexpr int KROW = Q8 ? D : 2 * D;
+    static constexpr int VROW = Q8 ? D / 2 : 2 * D;
+    static constexpr int KT = kBS * KROW;
+    static constexpr int VT = kBS * VROW;
+    static constexpr int KS = Q8 ? kBS * 2 : 0;
+    static constexpr int VS = Q8 ? kBS * NG * 2 : 0;
+    static constexpr int OFF_V = align_up(KT, 1024);
+    static constexpr int OFF_KS = OFF_V + align_up(VT, 16);
+    static constexpr int OFF_VS = OFF_KS + KS;
+    static constexpr int OFF_VZ = OFF_VS + VS;
+    static constexpr int TX = KT + VT + KS + 2 * VS;
+    static constexpr int STAGE = align_up(OFF_VZ + VS, 1024);
+    static constexpr int SCRATCH = 0;
+    static_assert(OFF_V % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1 KB alignment");
+
+    uint32_t qa[NKS][4];
+    float o[NNT][4];
+    float m_run[2], l_run[2];
+    float zacc[2][NG];
+    int lim[2];
+
+    static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
+                                                 const AttnParams& p, int kvh, int pb, uint64_t* bar) {
+        if constexpr (Q8) {
+            tma_load_2d(dst, km, kvh * D, pb * kBS, bar);
+            tma_load_2d(dst + OFF_V, vm, kvh * (D / 2), pb * kBS, bar);
+            const size_t meta = size_t(pb) * p.num_kv_heads + kvh;
+            bulk_load(dst + OFF_KS, reinterpret_cast<const uint8_t*>(p.k_scale) + meta * KS, KS, bar);
+            bulk_load(dst + OFF_VS, reinterpret_cast<const uint8_t*>(p.v_scale) + meta * VS, VS, bar);
+            bulk_load(dst + OFF_VZ, reinterpret_cast<const uint8_t*>(p.v_zero) + meta * VS, VS, bar);
+        } else {
+#pragma unroll
+            for (int b = 0; b < D / 64; ++b) {   // 128-byte boxes (64 dims) with the 128B swizzle
+                tma_load_2d(dst + b * 2048, km, kvh * D * 2 + b * 128, pb * kBS, bar);
+                tma_load_2d(dst + OFF_V + b * 2048, vm, kvh * D * 2 + b * 128, pb * kBS, bar);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void init(int) {}
+
+    // rows g and g+8 of the 16-row tile: row m = head (m / q_len), draft (m % q_len)
+    __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
+        const int g = lane >> 2, tid = lane & 3;
+        const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int m = g + 8 * r;
+            const bool valid = m < M;
+            const int h = valid ? m / QL : 0, j = valid ? m % QL : 0;
+            lim[r] = valid ? max(0, ctx - QL + j + 1) : 0;
+            const size_t qoff = ((size_t(s) * QL + j) * p.num_heads + kvh * G + h) * D;
+#pragma unroll
+            for (int kk = 0; kk < NKS; ++kk) {
+                uint32_t lo = 0, hi = 0;
+                if (valid) {
+                    if constexpr (Q8) {
+                        const int d0 = tid * (D / 4) + 4 * kk;   // lane's dims for k-step kk
+                        const float q0 = load_q(p.q, p.q_dtype, qoff + d0), q1 = load_q(p.q, p.q_dtype, qoff + d0 + 1);
+                        const float q2_ = load_q(p.q, p.q_dtype, qoff + d0 + 2),
+                                    q3 = load_q(p.q, p.q_dtype, qoff + d0 + 3);
+                        lo = pack2<false>(q0, q1);
+                        hi = pack2<false>(q2_, q3);
+                    } else {
+                        const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+                        lo = qw[(qoff + 16 * kk + 2 * tid) / 2];
+                        hi = qw[(qoff + 16 * kk + 8 + 2 * tid) / 2];
+                    }
+                }
+                qa[kk][r] = lo;
+                qa[kk][2 + r] = hi;
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < NNT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        m_run[0] = m_run[1] = -INFINITY;
+        l_run[0] = l_run[1] = 0.f;
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) zacc[0][gg] = zacc[1][gg] = 0.f;
+    }
+
+    __device__ __forceinline__ void block(const uint8_t* stg, int pos0, int ntok, uint8_t*, int lane) {
+        const int g = lane >> 2, tid = lane & 3;
+        const uint32_t stg_a = smem_addr(stg);
+        float sc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+        // ------------------------------------------------ S = Q K^T
+        if constexpr (Q8) {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int t = nt * 8 + g;
+                uint32_t w[NKS];
+#pragma unroll
+                for (int i = 0; i < D / 64; ++i) {
+                    const int c = tid * (D / 64) + i;
+                    const uint4 v = *reinterpret_cast<const uint4*>(stg + t * D + 16 * swz<D>(c, t));
+                    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+                }
+#pragma unroll
+                for (int kk = 0; kk < NKS; ++kk) {
+                    uint32_t b0, b1;
+                    s8x4_to_f16x4(w[kk], b0, b1);
+                    mma_f16(sc[nt], qa[kk], b0, b1);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const __half2 ks2 = *reinterpret_cast<const __half2*>(stg + OFF_KS + (nt * 8 + 2 * tid) * 2);
+                const float2 ks = __half22float2(ks2);
+                sc[nt][0] *= ks.x; sc[nt][1] *= ks.y; sc[nt][2] *= ks.x; sc[nt][3] *= ks.y;
+            }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+                for (int kp = 0; kp < NKS / 2; ++kp) {
+                    const int mi = lane >> 3, r = lane & 7;
+                    const int t = nt * 8 + r, c = 4 * kp + mi;           // 8-dim chunk c
+                    const uint32_t addr = stg_a + (c >> 3) * 2048 + t * 128 + 16 * swz<128>(c & 7, t);
+                    uint32_t R[4];
+                    ldsm_x4(addr, R);
+                    mma16816<BF>(sc[nt], qa[2 * kp], R[0], R[1]);
+                    mma16816<BF>(sc[nt], qa[2 * kp + 1], R[2], R[3]);
+                }
+            }
+        }
+        // ------------------------------------------------ scale, mask, online softmax (rows g, g+8)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int pos = pos0 + nt * 8 + 2 * tid + (e & 1);
+                sc[nt][e] = (pos < lim[e >> 1]) ? sc[nt][e] * scale_log2_ : -INFINITY;
+            }
+        float alpha[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float bm = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            const float mn = fmaxf(m_run[r], bm);
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            alpha[r] = exp2f(m_run[r] - mu);
+            float rs = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float pe = exp2f(sc[nt][2 * r + e] - mu);
+                    sc[nt][2 * r + e] = pe;
+                    rs += pe;
+                }
+            rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+            rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+            l_run[r] = l_run[r] * alpha[r] + rs;
+            m_run[r] = mn;
+        }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+            for (int n = 0; n < NNT; ++n) {
+                o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
+                o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
+            }
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                zacc[0][gg] *= alpha[0];
+                zacc[1][gg] *= alpha[1];
+            }
+        }
+        // ------------------------------------------------ O += P V
+        if constexpr (Q8) {
+            const int tk[4] = {2 * tid, 2 * tid + 1, 8 + 2 * tid, 9 + 2 * tid};
+            float sv[4][NG], zv[4][NG];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const bool valid = tk[i] < ntok;   // past the context: NaN metadata, kept out of the MMA
+                const __half* vs = reinterpret_cast<const __half*>(stg + OFF_VS) + tk[i] * NG;
+                const __half* vz = reinterpret_cast<const __half*>(stg + OFF_VZ) + tk[i] * NG;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg) {
+                    sv[i][gg] = valid ? __half2float(vs[gg]) : 0.f;
+                    zv[i][gg] = valid ? __half2float(vz[gg]) : 0.f;
+                }
+            }
+            uint32_t X[NG], Y[NG];
+#pragma unroll
+            for (int g0 = 0; g0 < NG; g0 += 2) {
+                const int mi = lane >> 3, r = lane & 7;
+                const int t = (mi & 1) * 8 + r, c = g0 + (mi >> 1);
+                const uint32_t addr = stg_a + OFF_V + t * (D / 2) + 16 * swz<D / 2>(c, t);
+                uint32_t R[4];
+                ldsm_x4_t(addr, R);
+                X[g0] = R[0]; Y[g0] = R[1]; X[g0 + 1] = R[2]; Y[g0 + 1] = R[3];
+            }
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                uint32_t a[4];
+                a[0] = pack2<false>(sc[0][0] * sv[0][gg], sc[0][1] * sv[1][gg]);
+                a[1] = pack2<false>(sc[0][2] * sv[0][gg], sc[0][3] * sv[1][gg]);
+                a[2] = pack2<false>(sc[1][0] * sv[2][gg], sc[1][1] * sv[3][gg]);
+                a[3] = pack2<false>(sc[1][2] * sv[2][gg], sc[1][3] * sv[3][gg]);
+                zacc[0][gg] += sc[0][0] * zv[0][gg] + sc[0][1] * zv[1][gg] + sc[1][0] * zv[2][gg] + sc[1][1] * zv[3][gg];
+                zacc[1][gg] += sc[0][2] * zv[0][gg] + sc[0][3] * zv[1][gg] + sc[1][2] * zv[2][gg] + sc[1][3] * zv[3][gg];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    mma_f16(o[4 * gg + i], a, u4pair_to_f16x2(X[gg], i), u4pair_to_f16x2(Y[gg], i));
+            }
+        } else {
+            // P as the A operand: bf16 keeps 8 significant bits, so P = hi + lo
+            // (two MMAs, P exact to ~2^-17); fp16's 11 bits are kept as one operand.
+            uint32_t a[4], alo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float x = sc[i >> 1][2 * (i & 1)], y = sc[i >> 1][2 * (i & 1) + 1];
+                a[i] = pack2<BF>(x, y);
+                if constexpr (BF) {
+                    const float hx = __uint_as_float(a[i] << 16), hy = __uint_as_float(a[i] & 0xffff0000u);
+                    alo[i] = pack2<BF>(x - hx, y - hy);
+                }
+            }
+            // V rows past the context may hold anything (NaN): zero them in the operand
+            const uint32_t m01 = (2 * tid < ntok ? 0x0000ffffu : 0u) | (2 * tid + 1 < ntok ? 0xffff0000u : 0u);
+            const uint32_t m23 = (8 + 2 * tid < ntok ? 0x0000ffffu : 0u) | (9 + 2 * tid < ntok ? 0xffff0000u : 0u);
+#pragma unroll
+            for (int np = 0; np < NNT / 2; ++np) {
+                const int mi = lane >> 3, r = lane & 7;
+                const int t = (mi & 1) * 8 + r, c = 2 * np + (mi >> 1);   // 8-dim chunk = n-tile
+                const uint32_t addr = stg_a + OFF_V + (c >> 3) * 2048 + t * 128 + 16 * swz<128>(c & 7, t);
+                uint32_t R[4];
+                ldsm_x4_t(addr, R);
+                if (ntok < kBS) {
+                    R[0] &= m01; R[1] &= m23; R[2] &= m01; R[3] &= m23;
+                }
+                mma16816<BF>(o[2 * np], a, R[0], R[1]);
+                mma16816<BF>(o[2 * np + 1], a, R[2], R[3]);
+                if constexpr (BF) {
+                    mma16816<BF>(o[2 * np], alo, R[0], R[1]);
+                    mma16816<BF>(o[2 * np + 1], alo, R[2], R[3]);
+                }
+            }
+        }
+    }
+
+    // K8/V4: add the V zero-point term sum_t p_t z_t (the same for every dim of a group)
+    __device__ __forceinline__ void finish(int lane) {
+        (void)lane;
+        if constexpr (Q8) {
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg)
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float z = zacc[r][gg];
+                    z += __shfl_xor_sync(0xffffffffu, z, 1);
+                    z += __shfl_xor_sync(0xffffffffu, z, 2);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        o[4 * gg + i][2 * r] += z;
+                        o[4 * gg + i][2 * r + 1] += z;
+                    }
+                }
+        }
+    }
+
+    __device__ __forceinline__ void store(float* ob, float* mw, float* lw, int M, int lane) const {
+        const int g = lane >> 2, tid = lane & 3;
+#pragma unroll
+        for (int n = 0; n < NNT; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = g + 8 * (e >> 1), col = 2 * tid + (e & 1);
+                const int d = Q8 ? 32 * (n >> 2) + 4 * col + (n & 3) : 8 * n + col;
+                if (m < M) ob[m * D + d] = o[n][e];
+            }
+        if (tid == 0) {
+            if (g < M) {
+                mw[g] = m_run[0];
+                lw[g] = l_run[0];
+            }
+            if (g + 8 < M) {
+                mw[g + 8] = m_run[1];
+                lw[g + 8] = l_run[1];
+            }
+        }
+    }
+
+    float scale_log2_;
+};
+
+// ---------------------------------------------------------------- work list
+
+__device__ __forceinline__ int seq_ctx(const AttnParams& p, int s) {
+    int c = p.context_lens[s];
+    const int cap = p.max_blocks * kBS;
+    return c < 0 ? 0 : (c > cap ? cap : c);
+}
+
+// units of sequence s: balanced = kv heads x blocks; split = kv heads x partitions
+__device__ __forceinline__ long long seq_units(const AttnParams& p, int nb) {
+    const int n = p.mode == kModeBalanced ? nb : (nb + p.partition_blocks - 1) / p.partition_blocks;
+    return (long long)p.num_kv_heads * n;
+}
+
+struct Seg {
+    int s, kvh, b0, b1, nb, ctx, part;
+    long long pair_start;   // balanced: first unit (block) of the pair
+    bool whole;             // the segment is the whole pair
+};
+
+// Iterates this CTA's segments in order.  Every warp runs its own copy; all
+// lanes of a warp hold the same state.
+struct SegIter {
+    long long u, u1;
+    int s;               // current sequence (split / balanced)
+    long long start;     // its first unit
+    long long n;         // its units
+    int nb, ctx;
+
+    __device__ __forceinline__ void load_seq(const AttnParams& p, int s_, long long start_) {
+        s = s_;
+        start = start_;
+        if (s < p.num_seqs) {
+            ctx = seq_ctx(p, s);
+            nb = (ctx + kBS - 1) / kBS;
+            n = seq_units(p, nb);
+        } else {
+            ctx = nb = 0;
+            n = 0;
+        }
+    }
+
+    __device__ __forceinline__ bool next(const AttnParams& p, Seg& g) {
+        if (u >= u1) return false;
+        const int Hkv = p.num_kv_heads;
+        if (p.mode == kModeSingle) {
+            g.s = int(u / Hkv);
+            g.kvh = int(u % Hkv);
+            g.ctx = seq_ctx(p, g.s);
+            g.nb = (g.ctx + kBS - 1) / kBS;
+            g.b0 = 0;
+            g.b1 = g.nb;
+            g.part = 0;
+            g.pair_start = 0;
+            g.whole = true;
+            u += 1;
+            return true;
+        }
+        while (s < p.num_seqs && u >= start + n) load_seq(p, s + 1, start + n);
+        if (s >= p.num_seqs) {
+            u = u1;
+            return false;
+        }
+        const long long local = u - start, per_pair = n / Hkv;
+        g.s = s;
+        g.kvh = int(local / per_pair);
+        const long long k = local % per_pair;
+        g.nb = nb;
+        g.ctx = ctx;
+        if (p.mode == kModeBalanced) {
+            const long long k1 = (per_pair < k + (u1 - u)) ? per_pair : k + (u1 - u);
+            g.b0 = int(k);
+            g.b1 = int(k1);
+            g.part = 0;
+            g.pair_start = start + g.kvh * per_pair;
+            g.whole = (k == 0 && k1 == per_pair);
+            u += k1 - k;
+        } else {
+            g.part = int(k);
+            g.b0 = int(k) * p.partition_blocks;
+            g.b1 = min(nb, g.b0 + p.partition_blocks);
+            g.pair_start = 0;
+            g.whole = false;
+            u += 1;
+        }
+        return true;
+    }
+};
+
+// Block-wide sum of the units of every sequence.
+__device__ long long cta_total_units(const AttnParams& p, long long* red) {
+    long long acc = 0;
+    for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) acc += seq_units(p, (seq_ctx(p, s) + kBS - 1) / kBS);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = acc;
+    __syncthreads();
+    long long tot = 0;
+    for (int w = 0; w < int(blockDim.x >> 5); ++w) tot += red[w];
+    __syncthreads();
+    return tot;
+}
+
+// Block-wide search for the sequence holding unit T: sets *s_out (num_seqs if
+// none) and *start_out (its first unit).
+__device__ void cta_locate(const AttnParams& p, long long T, long long* red, int* s_out, long long* start_out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    if (threadIdx.x == 0) {
+        *s_out = p.num_seqs;
+        *start_out = 0;
+    }
+    __syncthreads();
+    long long base = 0;
+    for (int r0 = 0; r0 < p.num_seqs; r0 += blockDim.x) {
+        const int s = r0 + threadIdx.x;
+        const long long u = (s < p.num_seqs) ? seq_units(p, (seq_ctx(p, s) + kBS - 1) / kBS) : 0;
+        long long incl = u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) red[warp] = incl;
+        __syncthreads();
+        long long before = 0, total = 0;
+        for (int w = 0; w < nw; ++w) {
+            if (w < warp) before += red[w];
+            total += red[w];
+        }
+        const long long hi = base + before + incl, lo = hi - u;
+        if (u > 0 && lo <= T && T < hi) {
+            *s_out = s;
+            *start_out = lo;
+        }
+        base += total;
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------- the kernel
+
+template <class Math>
+__global__ void __launch_bounds__(kThreads, 1)
+attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
+                 const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = p.stages;
+    const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL, D = p.head_dim;
+    const int H = p.num_heads, Hkv = p.num_kv_heads;
+    // shared-memory layout
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + size_t(S) * Math::STAGE);
+    uint64_t* empty = full + S;
+    int* poison = reinterpret_cast<int*>(empty + S);
+    long long* red = reinterpret_cast<long long*>(smem + align_up(S * Math::STAGE + 16 * S + 4 * S, 16));
+    int* flag = reinterpret_cast<int*>(red + 16);
+    float* mw = reinterpret_cast<float*>(flag + 4);                  // [kNCW][16]
+    float* lw = mw + kNCW * kMaxRows;                                 // [kNCW][16]
+    float* ob = lw + kNCW * kMaxRows;                                 // [kNCW][M][D]
+    uint8_t* scratch = reinterpret_cast<uint8_t*>(ob + size_t(kNCW) * M * D);   // [kNCW][SCRATCH]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
+
+    if (tid == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        fence_barrier_init();
+    }
+
+    // ---- this CTA's range of units
+    long long u0, u1, chunk;
+    int s0 = 0;
+    long long start0 = 0;
+    if (p.mode == kModeSingle) {
+        const long long total = (long long)p.num_seqs * Hkv;
+        chunk = (total + gridDim.x - 1) / gridDim.x;
+        u0 = blockIdx.x * chunk;
+        u1 = u0 + chunk < total ? u0 + chunk : total;
+        __syncthreads();
+    } else {
+        const long long total = cta_total_units(p, red);
+        chunk = (total + gridDim.x - 1) / gridDim.x;
+        if (p.mode == kModeBalanced && chunk < p.min_chunk) chunk = p.min_chunk;
+        u0 = blockIdx.x * chunk;
+        u1 = u0 + chunk < total ? u0 + chunk : total;
+        if (u0 < u1) {
+            cta_locate(p, u0, red, flag, &red[15]);   // flag[0] <- sequence, red[15] <- its first unit
+            s0 = flag[0];
+            start0 = red[15];
+        }
+        __syncthreads();
+    }
+    // context longer than its table: flagged once per sequence
+    for (int s = blockIdx.x * blockDim.x + tid; s < p.num_seqs; s += gridDim.x * blockDim.x)
+        if (p.context_lens[s] > p.max_blocks * kBS) flag_error(p.err, PKV_DEVERR_CAPACITY);
+
+    SegIter it;
+    it.u = u0;
+    it.u1 = u0 < u1 ? u1 : u0;
+    if (p.mode != kModeSingle) it.load_seq(p, s0, start0);
+
+    if (warp == kNCW) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            prefetch_tensormap(&k_map);
+            prefetch_tensormap(&v_map);
+        }
+        long long issued = 0;
+        Seg sg;
+        while (it.next(p, sg)) {
+            const int32_t* bt = p.block_tables + size_t(sg.s) * p.max_blocks;
+            const int n = sg.b1 - sg.b0;
+            for (int i0 = 0; i0 < n; i0 += 32) {
+                const int pbl = (i0 + lane < n) ? bt[sg.b0 + i0 + lane] : 0;
+                const int cnt = min(32, n - i0);
+                for (int jj = 0; jj < cnt; ++jj) {
+                    int pb = __shfl_sync(0xffffffffu, pbl, jj);
+                    if (lane == 0) {
+                        const int st = int(issued % S);
+                        const long long use = issued / S;
+                        if (use > 0 && !mbar_wait(&empty[st], uint32_t((use - 1) & 1)))
+                            flag_error(p.err, PKV_DEVERR_TIMEOUT);
+                        const int bad = (pb < 0 || pb >= p.num_blocks);
+                        if (bad) {
+                            flag_error(p.err, PKV_DEVERR_OOB_BLOCK);
+                            pb = 0;   // load a valid block; the consumer masks it out
+                        }
+                        poison[st] = bad;
+                        mbar_arrive_expect_tx(&full[st], Math::TX);
+                        Math::issue(smem + size_t(st) * Math::STAGE, &k_map, &v_map, p, sg.kvh, pb, &full[st]);
+                    }
+                    ++issued;
+                    __syncwarp();
+                }
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // balanced mode: sequences with nothing visible still get their zero rows
+    if (p.mode == kModeBalanced)
+        for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x)
+            if (seq_ctx(p, s) == 0)
+                for (int i = tid; i < QL * H * D; i += kNCW * 32)
+                    store_out(p.out, p.out_dtype, size_t(s) * QL * H * D + i, 0.f);
+
+    Math mth;
+    mth.init(lane);
+    if constexpr (Math::kTensor) mth.scale_log2_ = p.scale_log2;
+    uint8_t* my_scratch = scratch + warp * Math::SCRATCH;
+    long long jbase = 0;
+    Seg sg;
+    while (it.next(p, sg)) {
+        const int n = sg.b1 - sg.b0;
+        mth.begin(p, sg.s, sg.kvh, sg.ctx, lane);
+        for (int i = int((warp - jbase % kNCW + kNCW) % kNCW); i < n; i += kNCW) {
+            const long long j = jbase + i;
+            const int st = int(j % S);
+            const bool ok = mbar_wait(&full[st], uint32_t((j / S) & 1));
+            if (!ok && lane == 0) flag_error(p.err, PKV_DEVERR_TIMEOUT);
+            const int b = sg.b0 + i;
+            int ntok = (b == sg.nb - 1) ? sg.ctx - b * kBS : kBS;
+            if (!ok || poison[st]) ntok = 0;
+            if (ntok > 0) mth.block(smem + size_t(st) * Math::STAGE, b * kBS, ntok, my_scratch, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[st]);
+        }
+        jbase += n;
+        mth.finish(lane);
+
+        // ------------------------------------------------ merge the warps' states for this segment
+        mth.store(ob + size_t(warp) * M * D, mw + warp * kMaxRows, lw + warp * kMaxRows, M, lane);
+        named_barrier_sync(1, kNCW * 32);
+        const int pair = sg.s * Hkv + sg.kvh;
+        const bool piece = (p.mode == kModeBalanced) && !sg.whole;
+        const int slot = blockIdx.x + pair;
+        for (int idx = tid; idx < M * D; idx += kNCW * 32) {
+            const int m = idx / D, d = idx - (idx / D) * D;
+            float Mx = -INFINITY;
+#pragma unroll
+            for (int w2 = 0; w2 < kNCW; ++w2) Mx = fmaxf(Mx, mw[w2 * kMaxRows + m]);
+            float L = 0.f, O = 0.f;
+            if (Mx != -INFINITY) {
+#pragma unroll
+                for (int w2 = 0; w2 < kNCW; ++w2) {
+                    const float mm = mw[w2 * kMaxRows + m];
+                    if (mm != -INFINITY) {
+                        const float f = exp2f(mm - Mx);
+                        L = fmaf(lw[w2 * kMaxRows + m], f, L);
+                        O = fmaf(ob[(size_t(w2) * M + m) * D + d], f, O);
+                    }
+                }
+            }
+            const int h = m / QL, jq = m - (m / QL) * QL;
+            const size_t row = size_t(sg.s) * QL + jq;
+            const int hg = sg.kvh * G + h;
+            if (piece) {
+                p.part_o[(size_t(slot) * kMaxRows + m) * D + d] = O;
+                if (d == 0) {
+                    p.part_ml[(size_t(slot) * kMaxRows + m) * 2] = Mx;
+                    p.part_ml[(size_t(slot) * kMaxRows + m) * 2 + 1] = L;
+                }
+            } else if (p.mode == kModeSplit) {
+                const size_t pi = (row * H + hg) * p.max_partitions + sg.part;
+                p.tmp_out[pi * D + d] = (L > 0.f) ? O / L : 0.f;
+                if (d == 0) {
+                    p.max_logits[pi] = (L > 0.f) ? Mx * kLn2 : -INFINITY;
+                    p.exp_sums[pi] = L;
+                }
+            } else {
+                store_out(p.out, p.out_dtype, (row * H + hg) * D + d, (L > 0.f) ? O / L : 0.f);
+            }
+        }
+        if (piece) {
+            // the last piece of a pair to finish combines all of them (no waiting)
+            __threadfence();
+            named_barrier_sync(1, kNCW * 32);
+            const long long c_lo = sg.pair_start / chunk, c_hi = (sg.pair_start + sg.nb - 1) / chunk;
+            if (tid == 0) {
+                const int prev = atomicAdd(&p.counters[pair], 1);
+                flag[1] = (prev == int(c_hi - c_lo)) ? 1 : 0;
+            }
+            named_barrier_sync(1, kNCW * 32);
+            if (flag[1]) {
+                __threadfence();
+                for (int idx = tid; idx < M * D; idx += kNCW * 32) {
+                    const int m = idx / D, d = idx - (idx / D) * D;
+                    float Mx = -INFINITY;
+                    for (long long c = c_lo; c <= c_hi; ++c) {
+                        const size_t sl = size_t(c + pair) * kMaxRows + m;
+                        const float l = __ldcg(&p.part_ml[sl * 2 + 1]);
+                        if (l > 0.f) Mx = fmaxf(Mx, __ldcg(&p.part_ml[sl * 2]));
+                    }
+                    float L = 0.f, O = 0.f;
+                    if (Mx != -INFINITY)
+                        for (long long c = c_lo; c <= c_hi; ++c) {
+                            const size_t sl = size_t(c + pair) * kMaxRows + m;
+                            const float l = __ldcg(&p.part_ml[sl * 2 + 1]);
+                            if (l > 0.f) {
+                                const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - Mx);
+                                L = fmaf(l, f, L);
+                                O = fmaf(__ldcg(&p.part_o[sl * D + d]), f, O);
+                            }
+                        }
+                    const int h = m / QL, jq = m - (m / QL) * QL;
+                    store_out(p.out, p.out_dtype, ((size_t(sg.s) * QL + jq) * H + sg.kvh * G + h) * D + d,
+                              (L > 0.f) ? O / L : 0.f);
+                }
+                if (tid == 0) p.counters[pair] = 0;   // ready for the next launch
+            }
+        }
+        named_barrier_sync(1, kNCW * 32);   // the merge buffers are reused by the next segment
+    }
+}
+
+template <class Math>
+int smem_bytes(int stages, int M, int D) {
+    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + 16 * 8 + 16 + 2 * kNCW * kMaxRows * 4 +
+           kNCW * M * D * 4 + kNCW * Math::SCRATCH + 1024 + 64;
+}
+
+template <class Math>
+cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
+    static int num_sms = 0;
+    if (num_sms == 0) {
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const int M = (p.num_heads / p.num_kv_heads) * p.q_len;
+    const int base = smem_bytes<Math>(0, M, p.head_dim);
+    int stages = (kSmemLimit - base) / (Math::STAGE + 20);
+    if (stages > 9 * kNCW) stages = 9 * kNCW;
+    stages = stages / kNCW * kNCW;   // every stage always belongs to the same consumer warp
+    if (stages < kNCW) return cudaErrorInvalidConfiguration;
+    p.stages = stages;
+    const int smem = smem_bytes<Math>(stages, M, p.head_dim);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(attention_kernel<Math>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemLimit);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    long long units = (long long)p.num_seqs * p.num_kv_heads;   // single pass: pairs
+    if (p.mode != kModeSingle) units = (long long)p.num_seqs * p.num_kv_heads * p.max_blocks;   // upper bound
+    int grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
+    if (units < grid) grid = int(units < 1 ? 1 : units);
+    attention_kernel<Math><<<grid, kThreads, smem, stream>>>(km, vm, p);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t dispatch_cc(const AttnParams& p, int gqa, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+    switch (gqa) {
+        case 1: return launch_math<CcMath<T, D, 1>>(p, km, vm, st);
+        case 2: return launch_math<CcMath<T, D, 2>>(p, km, vm, st);
+        case 4: return launch_math<CcMath<T, D, 4>>(p, km, vm, st);
+        case 8: return launch_math<CcMath<T, D, 8>>(p, km, vm, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len) {
+    const bool shape = (head_dim == 64 || head_dim == 128) && (gqa == 1 || gqa == 2 || gqa == 4 || gqa == 8);
+    if (!shape || q_len < 1) return false;
+    if (attention_uses_tensor_cores(cache_kind, q_len)) return gqa * q_len <= kMaxRows;
+    return cache_kind == PKV_CACHE_F16 || cache_kind == PKV_CACHE_BF16;
+}
+
+bool attention_uses_tensor_cores(int cache_kind, int q_len) { return q_len > 1 || cache_kind == PKV_CACHE_K8V4; }
+
+cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& km, const CUtensorMap& vm,
+                             cudaStream_t stream) {
+    if (attention_uses_tensor_cores(cache_kind, p.q_len)) {
+        switch (cache_kind) {
+            case PKV_CACHE_K8V4:
+                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_K8V4, 128>>(p, km, vm, stream)
+                                         : launch_math<TcMath<PKV_CACHE_K8V4, 64>>(p, km, vm, stream);
+            case PKV_CACHE_BF16:
+                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_BF16, 128>>(p, km, vm, stream)
+                                         : launch_math<TcMath<PKV_CACHE_BF16, 64>>(p, km, vm, stream);
+            default:
+                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_F16, 128>>(p, km, vm, stream)
+                                         : launch_math<TcMath<PKV_CACHE_F16, 64>>(p, km, vm, stream);
+        }
+    }
+    if (cache_kind == PKV_CACHE_BF16)
+        return p.head_dim == 128 ? dispatch_cc<__nv_bfloat16, 128>(p, gqa, km, vm, stream)
+                                 : dispatch_cc<__nv_bfloat16, 64>(p, gqa, km, vm, stream);
+    return p.head_dim == 128 ? dispatch_cc<__half, 128>(p, gqa, km, vm, stream)
+                             : dispatch_cc<__half, 64>(p, gqa, km, vm, stream);
+}
+
+size_t balanced_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim) {
+    auto a256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t pairs = size_t(num_seqs) * size_t(num_kv_heads);
+    const size_t slots = size_t(kMaxGrid) + pairs;
+    return a256(slots * kMaxRows * size_t(head_dim) * 4) + a256(slots * kMaxRows * 2 * 4) + a256(pairs * 4);
+}
+
+}  // namespace pkv

@@ -39,16 +39,28 @@ struct AttnParams {
     int32_t num_seqs;
     int32_t max_blocks;
     uint32_t* err;
+    // persistent scheduling
+    int32_t mode;       // kModeSingle / kModeSplit / kModeBalanced
+    int32_t stages;     // shared-memory ring depth (a multiple of the consumer warps)
+    int32_t min_chunk;  // balanced: fewest 16-token blocks a CTA is given
+    float* part_o;      // balanced workspace: [slots, 16, head_dim] unnormalised partial outputs
+    float* part_ml;     // [slots, 16, 2] (max, sum) in base-2 units
+    int32_t* counters;  // [num_seqs * num_kv_heads] pieces finished per (sequence, kv head)
 };
 
-// Returns cudaSuccess or the launch error.  The grid is
-// (partitions, num_kv_heads, num_seqs); maps are K and V tile maps.
-cudaError_t launch_decode_cc(const AttnParams& p, int cache_kind, int gqa, const CUtensorMap& k_map,
-                             const CUtensorMap& v_map, int grid_parts, cudaStream_t stream);
-cudaError_t launch_decode_tc(const AttnParams& p, int cache_kind, int gqa, const CUtensorMap& k_map,
-                             const CUtensorMap& v_map, int grid_parts, cudaStream_t stream);
-bool decode_cc_supported(int cache_kind, int head_dim, int gqa);
-bool decode_tc_supported(int cache_kind, int head_dim, int gqa, int q_len);
+constexpr int kModeSingle = 0;
+constexpr int kModeSplit = 1;
+constexpr int kModeBalanced = 2;
+constexpr int kMaxGrid = 1024;  // CTAs of a persistent launch (bounds the balanced workspace)
+
+// Persistent attention kernel (attention.cu): one CTA per SM at most, the
+// (sequence, kv head, block) work list split into contiguous ranges.
+bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len);
+// Uses the CUDA-core math for fp16/bf16 with q_len 1, tensor cores otherwise.
+bool attention_uses_tensor_cores(int cache_kind, int q_len);
+cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& k_map,
+                             const CUtensorMap& v_map, cudaStream_t stream);
+size_t balanced_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim);
 
 struct ReduceParams {
     void* out;

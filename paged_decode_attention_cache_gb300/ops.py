@@ -75,6 +75,11 @@ def lib():
                                                 _P, _P, _P, _P]
         L.pkv_reduce.restype = st
         L.pkv_reduce.argtypes = [_P, ctypes.c_int, _P, _P, _P, _P, _I32, _I32, _I32, _I32, _P]
+        L.pkv_balanced_workspace_bytes.restype = ctypes.c_size_t
+        L.pkv_balanced_workspace_bytes.argtypes = [_I32, _I32, _I32]
+        L.pkv_paged_attention_balanced.restype = st
+        L.pkv_paged_attention_balanced.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
+                                                   _P, ctypes.c_size_t, _P, _P]
         L.pkv_gather_kv_cache.restype = st
         L.pkv_gather_kv_cache.argtypes = [_P, _P, _P, _P, _P, _P, _P]
         L.pkv_status_string.restype = ctypes.c_char_p
@@ -223,6 +228,27 @@ def pkv_reduce(out: torch.Tensor, tmp_out, max_logits, exp_sums, seqs: Seqs, par
     _check(lib().pkv_reduce(_ptr(out), _DT[out.dtype], _ptr(tmp_out), _ptr(max_logits), _ptr(exp_sums),
                             ctypes.byref(s), int(tmp_out.shape[1]), int(tmp_out.shape[3]), int(partition_size),
                             int(tmp_out.shape[2]), _stream(stream)))
+    return out
+
+
+def pkv_balanced_workspace_bytes(num_seqs: int, num_kv_heads: int, head_dim: int) -> int:
+    return int(lib().pkv_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim))
+
+
+def balanced_workspace(num_seqs: int, num_kv_heads: int, head_dim: int, device="cuda") -> torch.Tensor:
+    """Caller-side, zero-filled scratch for pkv_paged_attention_balanced (torch owns it)."""
+    n = pkv_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim)
+    return torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
+
+
+def pkv_paged_attention_balanced(out: torch.Tensor, q: torch.Tensor, scale: float, cache: Cache, seqs: Seqs,
+                                 workspace: torch.Tensor, err_flags: Optional[torch.Tensor] = None,
+                                 stream=None) -> torch.Tensor:
+    c, s = cache.c_struct(), seqs.c_struct()
+    _check(lib().pkv_paged_attention_balanced(_ptr(out), _DT[out.dtype], _ptr(q), _DT[q.dtype], int(q.shape[1]),
+                                              float(scale), ctypes.byref(c), ctypes.byref(s), _ptr(workspace),
+                                              int(workspace.numel() * workspace.element_size()),
+                                              _err_ptr(err_flags), _stream(stream)))
     return out
 
 

@@ -21,11 +21,22 @@ F16_NAN = 0x7E00
 
 class DecodeStep:
     def __init__(self, w: Workload, device: str = "cuda", partition_size: Optional[int] = None,
-                 out_dtype: Optional[torch.dtype] = None):
+                 out_dtype: Optional[torch.dtype] = None, schedule: Optional[str] = None):
+        """schedule: "single" (one CTA per sequence and kv head), "split"
+        (fixed partitions of partition_size tokens + LSE reduce) or "balanced"
+        (equal block ranges per SM, combine fused); by default split when the
+        workload names a partition size, else single."""
         self.w = w
         self.device = device
         dev = torch.device(device)
         self.partition_size = w.partition_size if partition_size is None else partition_size
+        if schedule is None:
+            schedule = "split" if self.partition_size > 0 else "single"
+        if schedule not in ("single", "split", "balanced"):
+            raise ValueError(schedule)
+        if schedule != "split":
+            self.partition_size = 0
+        self.schedule = schedule
         self.seqs = ops.Seqs(w.block_tables.to(dev).contiguous(), w.context_lens.to(dev).contiguous(), w.q_len)
         self.q = w.q.to(dev).contiguous()
         self.k_new = w.k_new.to(dev).contiguous()
@@ -47,11 +58,13 @@ class DecodeStep:
                                    w.v_cache.to(dev).contiguous().clone())
         dt = out_dtype or _TORCH[w.src_dtype]
         self.out = torch.empty((w.num_rows, w.num_heads, w.head_dim), dtype=dt, device=dev)
-        if self.partition_size > 0:
+        self.ws = None
+        self.bal_ws = None
+        if schedule == "split":
             nparts = -(-w.max_blocks * 16 // self.partition_size)
             self.ws = ops.split_workspace(w.num_rows, w.num_heads, w.head_dim, nparts, device=dev)
-        else:
-            self.ws = None
+        elif schedule == "balanced":
+            self.bal_ws = ops.balanced_workspace(w.num_seqs, w.num_kv_heads, w.head_dim, device=dev)
 
     @property
     def split(self) -> bool:
@@ -66,11 +79,14 @@ class DecodeStep:
             ops.pkv_reshape_and_cache(self.cache, self.k_new, self.v_new, self.slot_new, self.err, stream)
 
     def attend_phase1(self, stream=None):
-        """The dominant kernel: single-pass attention, or split-KV phase 1."""
+        """The dominant kernel: single-pass / balanced attention, or split-KV phase 1."""
         if self.split:
             tmp, ml, es = self.ws
             ops.pkv_paged_attention_split(tmp, ml, es, self.partition_size, self.q, self.w.scale, self.cache,
                                           self.seqs, self.err, stream)
+        elif self.schedule == "balanced":
+            ops.pkv_paged_attention_balanced(self.out, self.q, self.w.scale, self.cache, self.seqs, self.bal_ws,
+                                             self.err, stream)
         else:
             ops.pkv_paged_attention(self.out, self.q, self.w.scale, self.cache, self.seqs, self.err, stream)
 

@@ -44,7 +44,12 @@ def check_attention(got, ref, half_out):
 
 
 def run_step(w, partition=None, out_dtype=torch.float32):
-    st = DecodeStep(w, "cuda", partition_size=partition, out_dtype=out_dtype)
+    """partition: None (workload default), 0 (single pass), P > 0 (split + reduce)
+    or "bal" (balanced schedule with the fused combine)."""
+    if partition == "bal":
+        st = DecodeStep(w, "cuda", out_dtype=out_dtype, schedule="balanced")
+    else:
+        st = DecodeStep(w, "cuda", partition_size=partition, out_dtype=out_dtype)
     out = st.step()
     torch.cuda.synchronize()
     assert st.error_flags() == 0, f"device error flags {st.error_flags():#x}"
@@ -80,7 +85,7 @@ for D in (64, 128):
 
 
 @pytest.mark.parametrize("D,H,Hkv,dt", SMALL)
-@pytest.mark.parametrize("part", [0, 16, 48, 512])
+@pytest.mark.parametrize("part", [0, 16, 48, 512, "bal"])
 def test_small_shapes(D, H, Hkv, dt, part):
     ctx = [0, 1, 15, 16, 17, 511, 512, 513]
     w = W.build(name="t", seed=100 + D + H, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
@@ -107,7 +112,7 @@ def test_llama3_8b_batch8_full():
     w = W.llama3_8b_batch8(device="cuda")
     cs = oracle_cache_after_step(w)
     ref = oracle_attention(w, cs, threads=8)
-    for part in (256, 0):
+    for part in (256, 0, "bal"):
         st, got = run_step(w, part)
         check_attention(got, ref, False)
     # the write touched exactly the new tokens' slots
@@ -129,6 +134,35 @@ def test_long_context_32k_split_and_partials():
     lse_gpu = ml + np.log(es)
     lse_ref = pm + np.log(pl)
     np.testing.assert_allclose(lse_gpu, lse_ref, rtol=0, atol=1e-3)
+
+
+def test_long_context_32k_balanced():
+    w = W.long_context_32k(device="cuda")
+    ref = oracle_attention(w, threads=8)
+    _, got = run_step(w, "bal")
+    check_attention(got, ref, False)
+
+
+def test_balanced_many_ragged_sequences_and_workspace_reuse():
+    """Hundreds of short and empty sequences: CTAs hold pieces of several
+    sequences, pairs are cut across CTAs; the workspace counters return to zero
+    and a second call on the same workspace gives the same bits."""
+    rng = np.random.default_rng(3)
+    ctx = [int(x) for x in rng.integers(0, 700, 300)]
+    ctx[:5] = [0, 1, 16, 17, 0]
+    w = W.build(name="t", seed=51, context_lens=ctx, num_heads=16, num_kv_heads=4, head_dim=128, cache="bf16")
+    ref = oracle_attention(w, threads=16)
+    st = DecodeStep(w, "cuda", out_dtype=torch.float32, schedule="balanced")
+    out1 = st.step().clone()
+    torch.cuda.synchronize()
+    assert st.error_flags() == 0
+    check_attention(out1.double().cpu().numpy(), ref, False)
+    n_pairs = w.num_seqs * w.num_kv_heads
+    counters = st.bal_ws[-((n_pairs * 4 + 255) // 256 * 256):][: n_pairs * 4].view(torch.int32)
+    assert int(counters.abs().sum()) == 0
+    out2 = st.step()
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
 
 
 def test_reduce_kernel_on_oracle_partials():

@@ -28,7 +28,10 @@ def _built():
 
 
 def run(w, part, out_dtype=torch.float32):
-    st = DecodeStep(w, "cuda", partition_size=part, out_dtype=out_dtype)
+    if part == "bal":
+        st = DecodeStep(w, "cuda", out_dtype=out_dtype, schedule="balanced")
+    else:
+        st = DecodeStep(w, "cuda", partition_size=part, out_dtype=out_dtype)
     out = st.step()
     torch.cuda.synchronize()
     assert st.error_flags() == 0, f"device error flags {st.error_flags():#x}"
@@ -45,9 +48,9 @@ for D in (64, 128):
 
 @pytest.mark.parametrize("D,H,Hkv,ql", VERIFY)
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
-@pytest.mark.parametrize("part", [0, 32, 512])
+@pytest.mark.parametrize("part", [0, 32, 512, "bal"])
 def test_verify_small(D, H, Hkv, ql, dt, part):
-    if ql == 1 and part == 512:
+    if ql == 1 and part in (512, "bal"):
         pytest.skip("q_len 1 on fp16/bf16 runs the CUDA-core kernel")
     ctx = [2, 3, 4, 5, 16, 17, 100, 513]
     w = W.build(name="t", seed=200 + D + H + ql, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
@@ -59,7 +62,7 @@ def test_verify_small(D, H, Hkv, ql, dt, part):
 
 def test_verify_batch256_full_sampled_rows():
     w = W.verify_batch256(device="cuda")
-    st, got = run(w, 512)
+    st, got = run(w, "bal")
     cs = oracle_cache_after_step(w)
     # the drafts' K/V were written by the step: whole pool bit-exact
     assert np.array_equal(bits(st.cache.k), cs["k"]) and np.array_equal(bits(st.cache.v), cs["v"])
@@ -71,6 +74,8 @@ def test_verify_batch256_full_sampled_rows():
     check_attention(got[rows], ref[rows], False)
     _, got16 = run(w, 512, torch.bfloat16)
     check_attention(got16[rows], ref[rows], True)
+    _, got_single = run(w, 0)
+    check_attention(got_single[rows], ref[rows], False)
 
 
 # ---------------------------------------------------------------- K8/V4
@@ -82,7 +87,7 @@ for D in (64, 128):
 
 
 @pytest.mark.parametrize("D,H,Hkv,ql", K8)
-@pytest.mark.parametrize("part", [0, 48, 512])
+@pytest.mark.parametrize("part", [0, 48, 512, "bal"])
 def test_k8v4_small(D, H, Hkv, ql, part):
     ctx = [1, 5, 16, 17, 100, 511, 513] if ql == 1 else [4, 5, 17, 100, 513]
     w = W.build(name="t", seed=300 + D + H + ql, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
@@ -115,5 +120,6 @@ def test_k8v4_batch32_full_sampled_rows():
     ref = oracle_attention(w, cs, rows=rows, threads=16)
     err = np.abs(got[rows] - ref[rows]).max()
     assert err <= K8V4_ABS, f"max abs err {err:.3e}"
-    _, got1 = run(w, 0)
-    assert np.abs(got1[rows] - ref[rows]).max() <= K8V4_ABS
+    for part in (0, "bal"):
+        _, got1 = run(w, part)
+        assert np.abs(got1[rows] - ref[rows]).max() <= K8V4_ABS
