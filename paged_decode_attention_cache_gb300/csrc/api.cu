@@ -320,6 +320,9 @@ pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const vo
     CHECK_PTR(out, "out");
     if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
         return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (cache->num_kv_heads > pkv::kMaxGrid)
+        return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d above %d for the balanced schedule", cache->num_kv_heads,
+                    pkv::kMaxGrid);
     if (seqs->num_seqs == 0) return ok();
     const size_t need = pkv::balanced_workspace_bytes(seqs->num_seqs, cache->num_kv_heads, cache->head_dim);
     if (!workspace) return fail(PKV_ERR_INVALID_ARG, "workspace is NULL");

@@ -9,17 +9,21 @@
 // drafts, draft j seeing the history and drafts 0..j]:
 //   out[r, h] = sum_t softmax_t(scale * q[r,h] . K[t, h/g]) V[t, h/g]
 //
-// Work list.  The units of the batch are laid out sequence by sequence, kv head
-// by kv head, and CTA c takes units [c*chunk, (c+1)*chunk):
-//   single pass  unit = one (sequence, kv head) pair -> final output;
-//   split        unit = one partition of partition_size tokens of a pair ->
+// Work list.  Single pass: CTA c takes a contiguous range of the batch's
+// (sequence, kv head) pairs and writes final outputs.  Split and balanced: the
+// grid is Hkv lanes of L CTAs; CTA c serves kv head c % Hkv over the range
+// [i*chunk, (i+1)*chunk), i = c / Hkv, of the lane's unit list, laid out
+// sequence by sequence (so the Hkv CTAs of one range read the head slices of
+// the same blocks side by side, and each token row of the cache is fetched
+// from DRAM at once):
+//   split        unit = one partition of partition_size tokens ->
 //                normalised partial (o_p, m_p, l_p) for the LSE reduce;
-//   balanced     unit = one 16-token block of a pair, chunk = ceil(blocks/grid):
-//                every CTA streams the same number of blocks; a pair cut between
-//                CTAs leaves one unnormalised partial per piece in the
-//                workspace, and the CTA that finishes its pair's last piece
-//                (an atomic count, no waiting) combines the pieces by the same
-//                log-sum-exp identity and writes the output.
+//   balanced     unit = one 16-token block, chunk = ceil(blocks / L): every CTA
+//                streams the same number of blocks; a pair cut between CTAs
+//                leaves one unnormalised partial per piece in the workspace,
+//                and the CTA that finishes its pair's last piece (an atomic
+//                count, no waiting) combines the pieces by the same log-sum-exp
+//                identity and writes the output.
 //
 // CTA anatomy (256 threads).  Warp 7 produces: for each 16-token block it reads
 // the block table (32 entries per load), waits for a free ring stage and issues
@@ -661,15 +665,14 @@ __device__ __forceinline__ int seq_ctx(const AttnParams& p, int s) {
     return c < 0 ? 0 : (c > cap ? cap : c);
 }
 
-// units of sequence s: balanced = kv heads x blocks; split = kv heads x partitions
+// units of a sequence of nb blocks: balanced = blocks; split = partitions
 __device__ __forceinline__ long long seq_units(const AttnParams& p, int nb) {
-    const int n = p.mode == kModeBalanced ? nb : (nb + p.partition_blocks - 1) / p.partition_blocks;
-    return (long long)p.num_kv_heads * n;
+    return p.mode == kModeBalanced ? nb : (nb + p.partition_blocks - 1) / p.partition_blocks;
 }
 
 struct Seg {
     int s, kvh, b0, b1, nb, ctx, part;
-    long long pair_start;   // balanced: first unit (block) of the pair
+    long long pair_start;   // balanced: the sequence's first unit (block) in the lane's list
     bool whole;             // the segment is the whole pair
 };
 
@@ -677,6 +680,7 @@ struct Seg {
 // lanes of a warp hold the same state.
 struct SegIter {
     long long u, u1;
+    int kvh;             // split / balanced: the kv head of this CTA's lane
     int s;               // current sequence (split / balanced)
     long long start;     // its first unit
     long long n;         // its units
@@ -697,8 +701,8 @@ struct SegIter {
 
     __device__ __forceinline__ bool next(const AttnParams& p, Seg& g) {
         if (u >= u1) return false;
-        const int Hkv = p.num_kv_heads;
         if (p.mode == kModeSingle) {
+            const int Hkv = p.num_kv_heads;
             g.s = int(u / Hkv);
             g.kvh = int(u % Hkv);
             g.ctx = seq_ctx(p, g.s);
@@ -716,19 +720,18 @@ struct SegIter {
             u = u1;
             return false;
         }
-        const long long local = u - start, per_pair = n / Hkv;
+        const long long k = u - start;
         g.s = s;
-        g.kvh = int(local / per_pair);
-        const long long k = local % per_pair;
+        g.kvh = kvh;
         g.nb = nb;
         g.ctx = ctx;
         if (p.mode == kModeBalanced) {
-            const long long k1 = (per_pair < k + (u1 - u)) ? per_pair : k + (u1 - u);
+            const long long k1 = (n < k + (u1 - u)) ? n : k + (u1 - u);
             g.b0 = int(k);
             g.b1 = int(k1);
             g.part = 0;
-            g.pair_start = start + g.kvh * per_pair;
-            g.whole = (k == 0 && k1 == per_pair);
+            g.pair_start = start;
+            g.whole = (k == 0 && k1 == n);
             u += k1 - k;
         } else {
             g.part = int(k);
@@ -826,7 +829,11 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         fence_barrier_init();
     }
 
-    // ---- this CTA's range of units
+    // ---- this CTA's range of units.  Split / balanced: the grid is Hkv lanes of
+    // L CTAs; CTA c serves kv head c % Hkv over range c / Hkv of the lane's list,
+    // so CTAs c .. c+Hkv-1 stream the same blocks' head slices side by side and
+    // every 2*Hkv*D-byte token row of a block is read from DRAM at one time.
+    const int lane_kvh = blockIdx.x % Hkv, lane_idx = blockIdx.x / Hkv, nlanes = gridDim.x / Hkv;
     long long u0, u1, chunk;
     int s0 = 0;
     long long start0 = 0;
@@ -838,9 +845,9 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         __syncthreads();
     } else {
         const long long total = cta_total_units(p, red);
-        chunk = (total + gridDim.x - 1) / gridDim.x;
+        chunk = (total + nlanes - 1) / nlanes;
         if (p.mode == kModeBalanced && chunk < p.min_chunk) chunk = p.min_chunk;
-        u0 = blockIdx.x * chunk;
+        u0 = lane_idx * chunk;
         u1 = u0 + chunk < total ? u0 + chunk : total;
         if (u0 < u1) {
             cta_locate(p, u0, red, flag, &red[15]);   // flag[0] <- sequence, red[15] <- its first unit
@@ -856,6 +863,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     SegIter it;
     it.u = u0;
     it.u1 = u0 < u1 ? u1 : u0;
+    it.kvh = lane_kvh;
     if (p.mode != kModeSingle) it.load_seq(p, s0, start0);
 
     if (warp == kNCW) {
@@ -864,7 +872,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             prefetch_tensormap(&k_map);
             prefetch_tensormap(&v_map);
         }
-        long long issued = 0;
+        int issued = 0;   // blocks issued by this CTA
         Seg sg;
         while (it.next(p, sg)) {
             const int32_t* bt = p.block_tables + size_t(sg.s) * p.max_blocks;
@@ -875,8 +883,8 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 for (int jj = 0; jj < cnt; ++jj) {
                     int pb = __shfl_sync(0xffffffffu, pbl, jj);
                     if (lane == 0) {
-                        const int st = int(issued % S);
-                        const long long use = issued / S;
+                        const int st = issued % S;
+                        const int use = issued / S;
                         if (use > 0 && !mbar_wait(&empty[st], uint32_t((use - 1) & 1)))
                             flag_error(p.err, PKV_DEVERR_TIMEOUT);
                         const int bad = (pb < 0 || pb >= p.num_blocks);
@@ -908,14 +916,14 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     mth.init(lane);
     if constexpr (Math::kTensor) mth.scale_log2_ = p.scale_log2;
     uint8_t* my_scratch = scratch + warp * Math::SCRATCH;
-    long long jbase = 0;
+    int jbase = 0;   // blocks of this CTA before the current segment
     Seg sg;
     while (it.next(p, sg)) {
         const int n = sg.b1 - sg.b0;
         mth.begin(p, sg.s, sg.kvh, sg.ctx, lane);
-        for (int i = int((warp - jbase % kNCW + kNCW) % kNCW); i < n; i += kNCW) {
-            const long long j = jbase + i;
-            const int st = int(j % S);
+        for (int i = (warp - jbase % kNCW + kNCW) % kNCW; i < n; i += kNCW) {
+            const int j = jbase + i;
+            const int st = j % S;
             const bool ok = mbar_wait(&full[st], uint32_t((j / S) & 1));
             if (!ok && lane == 0) flag_error(p.err, PKV_DEVERR_TIMEOUT);
             const int b = sg.b0 + i;
@@ -933,7 +941,8 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         named_barrier_sync(1, kNCW * 32);
         const int pair = sg.s * Hkv + sg.kvh;
         const bool piece = (p.mode == kModeBalanced) && !sg.whole;
-        const int slot = blockIdx.x + pair;
+        // piece slot: unique because (lane_idx + s) grows along a lane's pieces
+        const int slot = (lane_idx + sg.s) * Hkv + sg.kvh;
         for (int idx = tid; idx < M * D; idx += kNCW * 32) {
             const int m = idx / D, d = idx - (idx / D) * D;
             float Mx = -INFINITY;
@@ -975,7 +984,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             // the last piece of a pair to finish combines all of them (no waiting)
             __threadfence();
             named_barrier_sync(1, kNCW * 32);
-            const long long c_lo = sg.pair_start / chunk, c_hi = (sg.pair_start + sg.nb - 1) / chunk;
+            const int c_lo = int(sg.pair_start / chunk), c_hi = int((sg.pair_start + sg.nb - 1) / chunk);
             if (tid == 0) {
                 const int prev = atomicAdd(&p.counters[pair], 1);
                 flag[1] = (prev == int(c_hi - c_lo)) ? 1 : 0;
@@ -986,15 +995,15 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 for (int idx = tid; idx < M * D; idx += kNCW * 32) {
                     const int m = idx / D, d = idx - (idx / D) * D;
                     float Mx = -INFINITY;
-                    for (long long c = c_lo; c <= c_hi; ++c) {
-                        const size_t sl = size_t(c + pair) * kMaxRows + m;
+                    for (int c = c_lo; c <= c_hi; ++c) {
+                        const size_t sl = size_t((c + sg.s) * Hkv + sg.kvh) * kMaxRows + m;
                         const float l = __ldcg(&p.part_ml[sl * 2 + 1]);
                         if (l > 0.f) Mx = fmaxf(Mx, __ldcg(&p.part_ml[sl * 2]));
                     }
                     float L = 0.f, O = 0.f;
                     if (Mx != -INFINITY)
-                        for (long long c = c_lo; c <= c_hi; ++c) {
-                            const size_t sl = size_t(c + pair) * kMaxRows + m;
+                        for (int c = c_lo; c <= c_hi; ++c) {
+                            const size_t sl = size_t((c + sg.s) * Hkv + sg.kvh) * kMaxRows + m;
                             const float l = __ldcg(&p.part_ml[sl * 2 + 1]);
                             if (l > 0.f) {
                                 const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - Mx);
@@ -1043,10 +1052,19 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    long long units = (long long)p.num_seqs * p.num_kv_heads;   // single pass: pairs
-    if (p.mode != kModeSingle) units = (long long)p.num_seqs * p.num_kv_heads * p.max_blocks;   // upper bound
-    int grid = num_sms < kMaxGrid ? num_sms : kMaxGrid;
-    if (units < grid) grid = int(units < 1 ? 1 : units);
+    const int cap = num_sms < kMaxGrid ? num_sms : kMaxGrid;
+    int grid;
+    if (p.mode == kModeSingle) {
+        const long long pairs = (long long)p.num_seqs * p.num_kv_heads;
+        grid = pairs < cap ? int(pairs < 1 ? 1 : pairs) : cap;
+    } else {
+        // Hkv lanes of L CTAs each (at least one lane)
+        int L = cap / p.num_kv_heads;
+        if (L < 1) L = 1;
+        const long long lane_units = (long long)p.num_seqs * p.max_blocks;   // upper bound of a lane's list
+        if (lane_units < L) L = int(lane_units < 1 ? 1 : lane_units);
+        grid = L * p.num_kv_heads;
+    }
     attention_kernel<Math><<<grid, kThreads, smem, stream>>>(km, vm, p);
     return cudaGetLastError();
 }
