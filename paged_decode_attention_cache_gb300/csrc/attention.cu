@@ -25,10 +25,11 @@
 //                count, no waiting) combines the pieces by the same log-sum-exp
 //                identity and writes the output.
 //
-// CTA anatomy (256 threads).  Warp 7 produces: for each 16-token block it reads
-// the block table (32 entries per load), waits for a free ring stage and issues
-// the TMA tile loads (and, for the K8/V4 cache, 1-D bulk copies of the block's
-// scales and zeros).  Warps 0-6 consume whole blocks round-robin, each with its
+// CTA anatomy (256 threads).  Warp 7 produces: up to 16 consecutive blocks per
+// pass, one per lane, each lane reading its block-table entry, waiting for its
+// ring stage to be free and issuing the TMA tile loads (and, for the K8/V4
+// cache, 1-D bulk copies of the block's scales and zeros) -- one lane issuing
+// block after block cannot keep an SM's HBM reads in flight.  Warps 0-6 consume whole blocks round-robin, each with its
 // own online-softmax state (running max m, sum l, unnormalised accumulator),
 // and merge through shared memory at the end of every segment (the part of a
 // pair that this CTA owns) while the producer already streams the next one.
@@ -56,9 +57,7 @@ namespace pkv {
 namespace {
 
 constexpr int kBS = 16;
-constexpr int kNCW = 7;                       // consumer warps (8 warps in all: one SM sub-partition
-                                              // then holds two, so a thread may use up to 255 registers)
-constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kMaxNCW = 11;                   // most consumer warps of any block math
 constexpr int kMaxRows = 16;                  // query rows per (sequence, kv head)
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -175,6 +174,10 @@ __device__ __forceinline__ void load_f2(const float2* src, float2 (&v)[N]) {
 template <typename T, int D, int G>
 struct CcMath {
     static constexpr bool kTensor = false;
+    // 11 consumer warps + the producer: 12 warps, three per SM sub-partition,
+    // which leaves 168 registers a thread -- enough for this math up to g = 4;
+    // g = 8 keeps 16 heads' q and accumulators and takes 7 (255 registers)
+    static constexpr int NCW = G >= 8 ? 7 : 11;
     static constexpr int CH = D / 8;                               // 16-byte chunks per row
     static constexpr int LPT = (G * D / 64 > 8) ? G * D / 64 : 8;  // lanes per token (QK)
     static constexpr int TPP = 32 / LPT;                           // tokens per pass
@@ -363,6 +366,9 @@ struct CcMath {
 template <int KIND, int D>
 struct TcMath {
     static constexpr bool kTensor = true;
+    // 7 consumer warps + the producer: 8 warps, two per SM sub-partition, so a
+    // thread may use up to 255 registers (the MMA fragments need ~230)
+    static constexpr int NCW = 7;
     static constexpr bool Q8 = KIND == PKV_CACHE_K8V4;
     static constexpr bool BF = KIND == PKV_CACHE_BF16;
     static constexpr int NG = D / 32;
@@ -686,11 +692,11 @@ struct SegIter {
     long long n;         // its units
     int nb, ctx;
 
-    __device__ __forceinline__ void load_seq(const AttnParams& p, int s_, long long start_) {
+    __device__ __forceinline__ void load_seq(const AttnParams& p, int s_, long long start_, int known_ctx = -1) {
         s = s_;
         start = start_;
         if (s < p.num_seqs) {
-            ctx = seq_ctx(p, s);
+            ctx = known_ctx >= 0 ? known_ctx : seq_ctx(p, s);
             nb = (ctx + kBS - 1) / kBS;
             n = seq_units(p, nb);
         } else {
@@ -745,30 +751,11 @@ struct SegIter {
     }
 };
 
-// Block-wide sum of the units of every sequence.
-__device__ long long cta_total_units(const AttnParams& p, long long* red) {
-    long long acc = 0;
-    for (int s = threadIdx.x; s < p.num_seqs; s += blockDim.x) acc += seq_units(p, (seq_ctx(p, s) + kBS - 1) / kBS);
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[warp] = acc;
-    __syncthreads();
-    long long tot = 0;
-    for (int w = 0; w < int(blockDim.x >> 5); ++w) tot += red[w];
-    __syncthreads();
-    return tot;
-}
-
 // Block-wide search for the sequence holding unit T: sets *s_out (num_seqs if
-// none) and *start_out (its first unit).
+// none) and *start_out (its first unit).  Used when the batch has more
+// sequences than the block has threads.
 __device__ void cta_locate(const AttnParams& p, long long T, long long* red, int* s_out, long long* start_out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    if (threadIdx.x == 0) {
-        *s_out = p.num_seqs;
-        *start_out = 0;
-    }
-    __syncthreads();
     long long base = 0;
     for (int r0 = 0; r0 < p.num_seqs; r0 += blockDim.x) {
         const int s = r0 + threadIdx.x;
@@ -796,12 +783,79 @@ __device__ void cta_locate(const AttnParams& p, long long T, long long* red, int
     }
 }
 
+// Block-wide plan of a split / balanced CTA: total units of the lane's list,
+// this CTA's range [u0, u1) and the sequence holding u0 (with its first unit
+// and context).  One pass over context_lens when the batch fits the block.
+struct Plan {
+    long long u0, u1, chunk, start0;
+    int s0, ctx0;
+};
+
+__device__ void cta_plan(const AttnParams& p, int lane_idx, int nlanes, long long* red, int* flag, Plan& pl) {
+    const int B = p.num_seqs, nthr = blockDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = nthr >> 5;
+    if (threadIdx.x == 0) {
+        flag[0] = B;       // s0
+        flag[2] = 0;       // ctx0 (-1: reload)
+        red[15] = 0;       // start0
+    }
+    long long base = 0, my_lo = 0, my_u = 0;
+    int my_s = B, my_ctx = 0;
+    for (int r0 = 0; r0 < B; r0 += nthr) {
+        const int s = r0 + threadIdx.x;
+        const int ctx = s < B ? seq_ctx(p, s) : 0;
+        const long long u = s < B ? seq_units(p, (ctx + kBS - 1) / kBS) : 0;
+        long long incl = u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) red[warp] = incl;
+        __syncthreads();
+        long long before = 0, total = 0;
+        for (int w = 0; w < nw; ++w) {
+            if (w < warp) before += red[w];
+            total += red[w];
+        }
+        my_lo = base + before + incl - u;
+        my_u = u;
+        my_s = s;
+        my_ctx = ctx;
+        base += total;
+        __syncthreads();
+    }
+    const long long total = base;
+    long long chunk = (total + nlanes - 1) / nlanes;
+    if (p.mode == kModeBalanced && chunk < p.min_chunk) chunk = p.min_chunk;
+    pl.chunk = chunk;
+    pl.u0 = lane_idx * chunk;
+    pl.u1 = pl.u0 + chunk < total ? pl.u0 + chunk : total;
+    if (pl.u0 < pl.u1) {
+        if (B <= nthr) {
+            if (my_u > 0 && my_lo <= pl.u0 && pl.u0 < my_lo + my_u) {
+                flag[0] = my_s;
+                flag[2] = my_ctx;
+                red[15] = my_lo;
+            }
+        } else {
+            if (threadIdx.x == 0) flag[2] = -1;
+            cta_locate(p, pl.u0, red + 0, flag, &red[15]);
+        }
+    }
+    __syncthreads();
+    pl.s0 = flag[0];
+    pl.ctx0 = flag[2];
+    pl.start0 = red[15];
+}
+
 // ---------------------------------------------------------------- the kernel
 
 template <class Math>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__((Math::NCW + 1) * 32, 1)
 attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                  const AttnParams p) {
+    constexpr int NCW = Math::NCW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = p.stages;
@@ -813,10 +867,10 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     int* poison = reinterpret_cast<int*>(empty + S);
     long long* red = reinterpret_cast<long long*>(smem + align_up(S * Math::STAGE + 16 * S + 4 * S, 16));
     int* flag = reinterpret_cast<int*>(red + 16);
-    float* mw = reinterpret_cast<float*>(flag + 4);                  // [kNCW][16]
-    float* lw = mw + kNCW * kMaxRows;                                 // [kNCW][16]
-    float* ob = lw + kNCW * kMaxRows;                                 // [kNCW][M][D]
-    uint8_t* scratch = reinterpret_cast<uint8_t*>(ob + size_t(kNCW) * M * D);   // [kNCW][SCRATCH]
+    float* mw = reinterpret_cast<float*>(flag + 4);                  // [NCW][16]
+    float* lw = mw + NCW * kMaxRows;                                  // [NCW][16]
+    float* ob = lw + NCW * kMaxRows;                                  // [NCW][M][D]
+    uint8_t* scratch = reinterpret_cast<uint8_t*>(ob + size_t(NCW) * M * D);   // [NCW][SCRATCH]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int tid = threadIdx.x;
@@ -834,83 +888,78 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     // so CTAs c .. c+Hkv-1 stream the same blocks' head slices side by side and
     // every 2*Hkv*D-byte token row of a block is read from DRAM at one time.
     const int lane_kvh = blockIdx.x % Hkv, lane_idx = blockIdx.x / Hkv, nlanes = gridDim.x / Hkv;
-    long long u0, u1, chunk;
-    int s0 = 0;
-    long long start0 = 0;
+    Plan pl;
     if (p.mode == kModeSingle) {
         const long long total = (long long)p.num_seqs * Hkv;
-        chunk = (total + gridDim.x - 1) / gridDim.x;
-        u0 = blockIdx.x * chunk;
-        u1 = u0 + chunk < total ? u0 + chunk : total;
+        pl.chunk = (total + gridDim.x - 1) / gridDim.x;
+        pl.u0 = blockIdx.x * pl.chunk;
+        pl.u1 = pl.u0 + pl.chunk < total ? pl.u0 + pl.chunk : total;
+        pl.s0 = 0;
+        pl.ctx0 = -1;
+        pl.start0 = 0;
         __syncthreads();
     } else {
-        const long long total = cta_total_units(p, red);
-        chunk = (total + nlanes - 1) / nlanes;
-        if (p.mode == kModeBalanced && chunk < p.min_chunk) chunk = p.min_chunk;
-        u0 = lane_idx * chunk;
-        u1 = u0 + chunk < total ? u0 + chunk : total;
-        if (u0 < u1) {
-            cta_locate(p, u0, red, flag, &red[15]);   // flag[0] <- sequence, red[15] <- its first unit
-            s0 = flag[0];
-            start0 = red[15];
-        }
-        __syncthreads();
+        cta_plan(p, lane_idx, nlanes, red, flag, pl);
     }
+    const long long chunk = pl.chunk;
     // context longer than its table: flagged once per sequence
     for (int s = blockIdx.x * blockDim.x + tid; s < p.num_seqs; s += gridDim.x * blockDim.x)
         if (p.context_lens[s] > p.max_blocks * kBS) flag_error(p.err, PKV_DEVERR_CAPACITY);
 
     SegIter it;
-    it.u = u0;
-    it.u1 = u0 < u1 ? u1 : u0;
+    it.u = pl.u0;
+    it.u1 = pl.u0 < pl.u1 ? pl.u1 : pl.u0;
     it.kvh = lane_kvh;
-    if (p.mode != kModeSingle) it.load_seq(p, s0, start0);
+    if (p.mode != kModeSingle) it.load_seq(p, pl.s0, pl.start0, pl.ctx0);
 
-    if (warp == kNCW) {
+    if (warp == NCW) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             prefetch_tensormap(&k_map);
             prefetch_tensormap(&v_map);
         }
+        // Up to `grp` consecutive blocks are issued per pass, one per lane: each
+        // lane waits for its own stage, reads its own block-table entry and
+        // issues its own copies, so the per-block chain (wait, expect_tx, TMA)
+        // of different blocks overlaps.  grp <= S: the previous use of every
+        // stage touched in a pass was issued by an earlier pass.
+        const int grp = S < 16 ? S : 16;
         int issued = 0;   // blocks issued by this CTA
         Seg sg;
         while (it.next(p, sg)) {
             const int32_t* bt = p.block_tables + size_t(sg.s) * p.max_blocks;
             const int n = sg.b1 - sg.b0;
-            for (int i0 = 0; i0 < n; i0 += 32) {
-                const int pbl = (i0 + lane < n) ? bt[sg.b0 + i0 + lane] : 0;
-                const int cnt = min(32, n - i0);
-                for (int jj = 0; jj < cnt; ++jj) {
-                    int pb = __shfl_sync(0xffffffffu, pbl, jj);
-                    if (lane == 0) {
-                        const int st = issued % S;
-                        const int use = issued / S;
-                        if (use > 0 && !mbar_wait(&empty[st], uint32_t((use - 1) & 1)))
-                            flag_error(p.err, PKV_DEVERR_TIMEOUT);
-                        const int bad = (pb < 0 || pb >= p.num_blocks);
-                        if (bad) {
-                            flag_error(p.err, PKV_DEVERR_OOB_BLOCK);
-                            pb = 0;   // load a valid block; the consumer masks it out
-                        }
-                        poison[st] = bad;
-                        mbar_arrive_expect_tx(&full[st], Math::TX);
-                        Math::issue(smem + size_t(st) * Math::STAGE, &k_map, &v_map, p, sg.kvh, pb, &full[st]);
+            for (int i0 = 0; i0 < n; i0 += grp) {
+                if (lane < grp && i0 + lane < n) {
+                    int pb = bt[sg.b0 + i0 + lane];
+                    const int j = issued + lane;
+                    const int st = j % S;
+                    const int use = j / S;
+                    if (use > 0 && !mbar_wait(&empty[st], uint32_t((use - 1) & 1)))
+                        flag_error(p.err, PKV_DEVERR_TIMEOUT);
+                    const int bad = (pb < 0 || pb >= p.num_blocks);
+                    if (bad) {
+                        flag_error(p.err, PKV_DEVERR_OOB_BLOCK);
+                        pb = 0;   // load a valid block; the consumer masks it out
                     }
-                    ++issued;
-                    __syncwarp();
+                    poison[st] = bad;
+                    mbar_arrive_expect_tx(&full[st], Math::TX);
+                    Math::issue(smem + size_t(st) * Math::STAGE, &k_map, &v_map, p, sg.kvh, pb, &full[st]);
                 }
+                issued += min(grp, n - i0);
+                __syncwarp();
             }
         }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
+    constexpr int CT = NCW * 32;   // consumer threads
     // balanced mode: sequences with nothing visible still get their zero rows
     if (p.mode == kModeBalanced)
         for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x)
             if (seq_ctx(p, s) == 0)
-                for (int i = tid; i < QL * H * D; i += kNCW * 32)
-                    store_out(p.out, p.out_dtype, size_t(s) * QL * H * D + i, 0.f);
+                for (int i = tid; i < QL * H * D; i += CT) store_out(p.out, p.out_dtype, size_t(s) * QL * H * D + i, 0.f);
 
     Math mth;
     mth.init(lane);
@@ -921,7 +970,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     while (it.next(p, sg)) {
         const int n = sg.b1 - sg.b0;
         mth.begin(p, sg.s, sg.kvh, sg.ctx, lane);
-        for (int i = (warp - jbase % kNCW + kNCW) % kNCW; i < n; i += kNCW) {
+        for (int i = (warp - jbase % NCW + NCW) % NCW; i < n; i += NCW) {
             const int j = jbase + i;
             const int st = j % S;
             const bool ok = mbar_wait(&full[st], uint32_t((j / S) & 1));
@@ -938,20 +987,20 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 
         // ------------------------------------------------ merge the warps' states for this segment
         mth.store(ob + size_t(warp) * M * D, mw + warp * kMaxRows, lw + warp * kMaxRows, M, lane);
-        named_barrier_sync(1, kNCW * 32);
+        named_barrier_sync(1, CT);
         const int pair = sg.s * Hkv + sg.kvh;
         const bool piece = (p.mode == kModeBalanced) && !sg.whole;
         // piece slot: unique because (lane_idx + s) grows along a lane's pieces
         const int slot = (lane_idx + sg.s) * Hkv + sg.kvh;
-        for (int idx = tid; idx < M * D; idx += kNCW * 32) {
+        for (int idx = tid; idx < M * D; idx += CT) {
             const int m = idx / D, d = idx - (idx / D) * D;
             float Mx = -INFINITY;
 #pragma unroll
-            for (int w2 = 0; w2 < kNCW; ++w2) Mx = fmaxf(Mx, mw[w2 * kMaxRows + m]);
+            for (int w2 = 0; w2 < NCW; ++w2) Mx = fmaxf(Mx, mw[w2 * kMaxRows + m]);
             float L = 0.f, O = 0.f;
             if (Mx != -INFINITY) {
 #pragma unroll
-                for (int w2 = 0; w2 < kNCW; ++w2) {
+                for (int w2 = 0; w2 < NCW; ++w2) {
                     const float mm = mw[w2 * kMaxRows + m];
                     if (mm != -INFINITY) {
                         const float f = exp2f(mm - Mx);
@@ -983,34 +1032,57 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         if (piece) {
             // the last piece of a pair to finish combines all of them (no waiting)
             __threadfence();
-            named_barrier_sync(1, kNCW * 32);
+            named_barrier_sync(1, CT);
             const int c_lo = int(sg.pair_start / chunk), c_hi = int((sg.pair_start + sg.nb - 1) / chunk);
+            const int np = c_hi - c_lo + 1;
             if (tid == 0) {
                 const int prev = atomicAdd(&p.counters[pair], 1);
-                flag[1] = (prev == int(c_hi - c_lo)) ? 1 : 0;
+                flag[1] = (prev == np - 1) ? 1 : 0;
             }
-            named_barrier_sync(1, kNCW * 32);
+            named_barrier_sync(1, CT);
             if (flag[1]) {
                 __threadfence();
-                for (int idx = tid; idx < M * D; idx += kNCW * 32) {
-                    const int m = idx / D, d = idx - (idx / D) * D;
+                // stage every piece's (max, sum) of every row, then the row's weights
+                float* pm = ob;                    // [np][M] maxima, then weights
+                float* pw = ob + np * M;           // [np][M] sums
+                float* rl = pw + np * M;           // [M] combined sums
+                for (int t = tid; t < np * M; t += CT) {
+                    const int c = c_lo + t / M, m = t - (t / M) * M;
+                    const size_t sl = size_t((c + sg.s) * Hkv + sg.kvh) * kMaxRows + m;
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl);
+                    pm[t] = ml.x;
+                    pw[t] = ml.y;
+                }
+                named_barrier_sync(1, CT);
+                for (int m = tid; m < M; m += CT) {
                     float Mx = -INFINITY;
-                    for (int c = c_lo; c <= c_hi; ++c) {
-                        const size_t sl = size_t((c + sg.s) * Hkv + sg.kvh) * kMaxRows + m;
-                        const float l = __ldcg(&p.part_ml[sl * 2 + 1]);
-                        if (l > 0.f) Mx = fmaxf(Mx, __ldcg(&p.part_ml[sl * 2]));
+                    for (int c = 0; c < np; ++c)
+                        if (pw[c * M + m] > 0.f) Mx = fmaxf(Mx, pm[c * M + m]);
+                    float L = 0.f;
+                    for (int c = 0; c < np; ++c) {
+                        const float w = (pw[c * M + m] > 0.f) ? pw[c * M + m] * exp2f(pm[c * M + m] - Mx) : 0.f;
+                        pm[c * M + m] = w;
+                        L += w;
                     }
-                    float L = 0.f, O = 0.f;
-                    if (Mx != -INFINITY)
-                        for (int c = c_lo; c <= c_hi; ++c) {
-                            const size_t sl = size_t((c + sg.s) * Hkv + sg.kvh) * kMaxRows + m;
-                            const float l = __ldcg(&p.part_ml[sl * 2 + 1]);
-                            if (l > 0.f) {
-                                const float f = exp2f(__ldcg(&p.part_ml[sl * 2]) - Mx);
-                                L = fmaf(l, f, L);
-                                O = fmaf(__ldcg(&p.part_o[sl * D + d]), f, O);
-                            }
-                        }
+                    rl[m] = L;
+                }
+                named_barrier_sync(1, CT);
+                for (int idx = tid; idx < M * D; idx += CT) {
+                    const int m = idx / D, d = idx - (idx / D) * D;
+                    float O = 0.f;
+                    int c = 0;
+                    for (; c + 4 <= np; c += 4) {   // four independent loads in flight
+                        float v[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            v[u] = __ldcg(&p.part_o[(size_t((c_lo + c + u + sg.s) * Hkv + sg.kvh) * kMaxRows + m) * D + d]);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) O = fmaf(pm[(c + u) * M + m], v[u], O);
+                    }
+                    for (; c < np; ++c)
+                        O = fmaf(pm[c * M + m],
+                                 __ldcg(&p.part_o[(size_t((c_lo + c + sg.s) * Hkv + sg.kvh) * kMaxRows + m) * D + d]), O);
+                    const float L = rl[m];
                     const int h = m / QL, jq = m - (m / QL) * QL;
                     store_out(p.out, p.out_dtype, ((size_t(sg.s) * QL + jq) * H + sg.kvh * G + h) * D + d,
                               (L > 0.f) ? O / L : 0.f);
@@ -1018,14 +1090,15 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 if (tid == 0) p.counters[pair] = 0;   // ready for the next launch
             }
         }
-        named_barrier_sync(1, kNCW * 32);   // the merge buffers are reused by the next segment
+        named_barrier_sync(1, CT);   // the merge buffers are reused by the next segment
     }
 }
 
 template <class Math>
 int smem_bytes(int stages, int M, int D) {
-    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + 16 * 8 + 16 + 2 * kNCW * kMaxRows * 4 +
-           kNCW * M * D * 4 + kNCW * Math::SCRATCH + 1024 + 64;
+    constexpr int NCW = Math::NCW;
+    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + 16 * 8 + 16 + 2 * NCW * kMaxRows * 4 +
+           NCW * M * D * 4 + NCW * Math::SCRATCH + 1024 + 64;
 }
 
 template <class Math>
@@ -1040,9 +1113,9 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
     const int M = (p.num_heads / p.num_kv_heads) * p.q_len;
     const int base = smem_bytes<Math>(0, M, p.head_dim);
     int stages = (kSmemLimit - base) / (Math::STAGE + 20);
-    if (stages > 9 * kNCW) stages = 9 * kNCW;
-    stages = stages / kNCW * kNCW;   // every stage always belongs to the same consumer warp
-    if (stages < kNCW) return cudaErrorInvalidConfiguration;
+    if (stages > 9 * Math::NCW) stages = 9 * Math::NCW;
+    stages = stages / Math::NCW * Math::NCW;   // every stage always belongs to the same consumer warp
+    if (stages < Math::NCW) return cudaErrorInvalidConfiguration;
     p.stages = stages;
     const int smem = smem_bytes<Math>(stages, M, p.head_dim);
     static bool attr_set = false;
@@ -1065,7 +1138,7 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
         if (lane_units < L) L = int(lane_units < 1 ? 1 : lane_units);
         grid = L * p.num_kv_heads;
     }
-    attention_kernel<Math><<<grid, kThreads, smem, stream>>>(km, vm, p);
+    attention_kernel<Math><<<grid, (Math::NCW + 1) * 32, smem, stream>>>(km, vm, p);
     return cudaGetLastError();
 }
 
