@@ -1054,15 +1054,17 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                     pw[t] = ml.y;
                 }
                 named_barrier_sync(1, CT);
+                // pieces hold unnormalised sums relative to their own max m_c:
+                // O = sum_c 2^(m_c - M) O_c, L = sum_c 2^(m_c - M) l_c
                 for (int m = tid; m < M; m += CT) {
                     float Mx = -INFINITY;
                     for (int c = 0; c < np; ++c)
                         if (pw[c * M + m] > 0.f) Mx = fmaxf(Mx, pm[c * M + m]);
                     float L = 0.f;
                     for (int c = 0; c < np; ++c) {
-                        const float w = (pw[c * M + m] > 0.f) ? pw[c * M + m] * exp2f(pm[c * M + m] - Mx) : 0.f;
-                        pm[c * M + m] = w;
-                        L += w;
+                        const float f = (pw[c * M + m] > 0.f) ? exp2f(pm[c * M + m] - Mx) : 0.f;
+                        pm[c * M + m] = f;
+                        L = fmaf(pw[c * M + m], f, L);
                     }
                     rl[m] = L;
                 }
