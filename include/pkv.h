@@ -248,6 +248,36 @@ pkv_status pkv_paged_attention_balanced(void *out, pkv_dtype out_dtype, const vo
                                         const pkv_seqs *seqs, void *workspace, size_t workspace_bytes,
                                         uint32_t *err_flags, pkv_stream_t stream);
 
+/* Bytes of device memory the library image reserves for
+ * pkv_paged_attention_balanced_noalloc (32 MiB). */
+#define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * pkv_paged_attention_balanced without a caller-provided workspace.  The pages
+ * have no counterpart of this entry point: it exists for callers that cannot
+ * allocate device memory themselves -- a plain C host program that links only
+ * this library and owns no device allocator, or a serving loop that must not
+ * allocate after start-up because its memory budget is fixed.  Its scratch is a
+ * static array of PKV_NOALLOC_SCRATCH_BYTES inside the library's device image,
+ * which every GPU that loads the library holds until the process exits.
+ *   Limit: pkv_balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim) must
+ *   not exceed PKV_NOALLOC_SCRATCH_BYTES (about 3000 (sequence, kv head) pairs
+ *   at head_dim 128, 6900 at head_dim 64); a larger batch returns
+ *   PKV_ERR_INVALID_ARG with an explanation and launches nothing.
+ *   Set-up: the first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents; each call clears the part that must start at zero (one
+ *   cudaMemsetAsync on `stream`, no allocation).  Calls that overlap on the GPU
+ *   (other streams, other host threads) race on the array and give wrong
+ *   results: serialise them.
+ * Allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine.
+ * Arguments and result as for pkv_paged_attention_balanced.
+ */
+pkv_status pkv_paged_attention_balanced_noalloc(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                                int32_t num_heads, float scale, const pkv_cache *cache,
+                                                const pkv_seqs *seqs, uint32_t *err_flags, pkv_stream_t stream);
+
 /*
  * Copy every visible token of every sequence back to contiguous storage
  * [METAL names the gather_kv_cache kernel].

@@ -347,6 +347,97 @@ pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const vo
     return attn_launch(p, cache, gqa, stream);
 }
 
+}  // extern "C"
+
+// ---------------------------------------------------------------- the allocation-free variant
+// Scratch of pkv_paged_attention_balanced_noalloc: one array in the library's
+// own device image, so a caller that cannot allocate device memory still gets
+// the balanced schedule.  Every GPU that loads the library holds it until the
+// process exits.  Host code must not use the symbol as a device address; the
+// address is looked up once per device below.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(PKV_NOALLOC_SCRATCH_BYTES);
+static_assert(kNoAllocScratchBytes % 256 == 0, "scratch size must keep 256-byte alignment");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 256;
+
+// Device address of g_noalloc_scratch on the current device, looked up on the
+// first call made with that device current (cudaGetSymbolAddress).
+void* noalloc_scratch(pkv_status* st) {
+    static std::mutex mu;
+    static void* addr[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) {
+        *st = fail(PKV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+        return nullptr;
+    }
+    if (dev < 0 || dev >= kMaxDevices) {
+        *st = fail(PKV_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices - 1);
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        if (e != cudaSuccess || ptr == nullptr) {
+            *st = fail(PKV_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
+            return nullptr;
+        }
+        addr[dev] = ptr;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_balanced_noalloc(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
+                                                int32_t num_heads, float scale, const pkv_cache* cache,
+                                                const pkv_seqs* seqs, uint32_t* err_flags, pkv_stream_t stream) {
+    pkv::AttnParams p;
+    int gqa = 0;
+    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
+    if (st != PKV_OK) return st;
+    CHECK_PTR(out, "out");
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
+        return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if (cache->num_kv_heads > pkv::kMaxGrid)
+        return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d above %d for the balanced schedule", cache->num_kv_heads,
+                    pkv::kMaxGrid);
+    if (seqs->num_seqs == 0) return ok();
+    const size_t need = pkv::balanced_workspace_bytes(seqs->num_seqs, cache->num_kv_heads, cache->head_dim);
+    if (need > kNoAllocScratchBytes)
+        return fail(PKV_ERR_INVALID_ARG,
+                    "batch too large for the static scratch: %d sequences x %d kv heads at head_dim %d need %zu "
+                    "bytes, the library holds %zu (use pkv_paged_attention_balanced with your own workspace)",
+                    seqs->num_seqs, cache->num_kv_heads, cache->head_dim, need, kNoAllocScratchBytes);
+    void* ws = noalloc_scratch(&st);
+    if (!ws) return st;
+    const size_t pairs = size_t(seqs->num_seqs) * size_t(cache->num_kv_heads);
+    const size_t slots = size_t(pkv::kMaxGrid) + pairs;
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    p.part_o = reinterpret_cast<float*>(w);
+    w += align256(slots * 16 * size_t(cache->head_dim) * 4);
+    p.part_ml = reinterpret_cast<float*>(w);
+    w += align256(slots * 16 * 2 * 4);
+    p.counters = reinterpret_cast<int32_t*>(w);
+    // the array keeps whatever the previous call left: the piece counters must
+    // start at zero (partials are always written before they are read)
+    cudaError_t e = cudaMemsetAsync(p.counters, 0, pairs * sizeof(int32_t), reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_result(e, "clearing the static scratch counters");
+    p.out = out;
+    p.out_dtype = out_dtype;
+    p.partition_blocks = seqs->max_blocks_per_seq;
+    p.max_partitions = 1;
+    p.mode = pkv::kModeBalanced;
+    p.min_chunk = 8;
+    return attn_launch(p, cache, gqa, stream);
+}
+
 pkv_status pkv_reduce(void* out, pkv_dtype out_dtype, const float* tmp_out, const float* max_logits,
                       const float* exp_sums, const pkv_seqs* seqs, int32_t num_heads, int32_t head_dim,
                       int32_t partition_size, int32_t max_partitions, pkv_stream_t stream) {

@@ -57,7 +57,6 @@ namespace pkv {
 namespace {
 
 constexpr int kBS = 16;
-constexpr int kMaxNCW = 11;                   // most consumer warps of any block math
 constexpr int kMaxRows = 16;                  // query rows per (sequence, kv head)
 constexpr int kSmemLimit = 227 * 1024;
 

@@ -80,6 +80,9 @@ def lib():
         L.pkv_paged_attention_balanced.restype = st
         L.pkv_paged_attention_balanced.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
                                                    _P, ctypes.c_size_t, _P, _P]
+        L.pkv_paged_attention_balanced_noalloc.restype = st
+        L.pkv_paged_attention_balanced_noalloc.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float,
+                                                           _P, _P, _P, _P]
         L.pkv_gather_kv_cache.restype = st
         L.pkv_gather_kv_cache.argtypes = [_P, _P, _P, _P, _P, _P, _P]
         L.pkv_status_string.restype = ctypes.c_char_p
@@ -249,6 +252,19 @@ def pkv_paged_attention_balanced(out: torch.Tensor, q: torch.Tensor, scale: floa
                                               float(scale), ctypes.byref(c), ctypes.byref(s), _ptr(workspace),
                                               int(workspace.numel() * workspace.element_size()),
                                               _err_ptr(err_flags), _stream(stream)))
+    return out
+
+
+def pkv_paged_attention_balanced_noalloc(out: torch.Tensor, q: torch.Tensor, scale: float, cache: Cache,
+                                         seqs: Seqs, err_flags: Optional[torch.Tensor] = None,
+                                         stream=None) -> torch.Tensor:
+    """The balanced schedule with the library's own static scratch: for callers
+    that cannot allocate device memory (see include/pkv.h for the size limit and
+    the rule that calls sharing a device must not overlap)."""
+    c, s = cache.c_struct(), seqs.c_struct()
+    _check(lib().pkv_paged_attention_balanced_noalloc(_ptr(out), _DT[out.dtype], _ptr(q), _DT[q.dtype],
+                                                      int(q.shape[1]), float(scale), ctypes.byref(c),
+                                                      ctypes.byref(s), _err_ptr(err_flags), _stream(stream)))
     return out
 
 
