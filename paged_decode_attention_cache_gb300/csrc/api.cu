@@ -116,15 +116,33 @@ pkv_status tile_map(CUtensorMap* map, void* base, int64_t rows, int64_t row_byte
     return PKV_OK;
 }
 
+// A 3-D view for the tensor-core tiles of fp16/bf16 caches: {128-byte chunk,
+// token slot, chunk index across the row}.  One box {128, 16, D/64} is a kv
+// head's 16 rows, landing chunk-major as D/64 sub-tiles of 16 x 128 bytes (the
+// layout the 128B swizzle and ldmatrix want), in a single copy operation.
+pkv_status chunk_map(CUtensorMap* map, void* base, int64_t rows, int64_t row_bytes, int head_dim) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    cuuint64_t dims[3] = {128u, cuuint64_t(rows), cuuint64_t(row_bytes / 128)};
+    cuuint64_t strides[2] = {cuuint64_t(row_bytes), 128u};
+    cuuint32_t box[3] = {128u, 16u, cuuint32_t(head_dim / 64)};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", int(r));
+    return PKV_OK;
+}
+
 CUtensorMapSwizzle swizzle_for(int row_bytes) {
     return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                             : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
 // CUDA-core kernel: one box per tile (16 rows x one kv head), no swizzle.
-// Tensor-core kernel: swizzled boxes of at most 128 bytes per row, so that the
-// ldmatrix / 128-bit reads of a tile are conflict-free (fp16/bf16: 64-dim boxes
-// with the 128B swizzle; K8: the whole D-byte row; V4: the whole D/2-byte row).
+// Tensor-core kernel: swizzled rows of at most 128 bytes, so that the ldmatrix /
+// 128-bit reads of a tile are conflict-free (fp16/bf16: 64-dim chunks with the
+// 128B swizzle, one 3-D box; K8: the whole D-byte row; V4: the whole D/2-byte row).
 pkv_status cache_maps(const pkv_cache* c, CUtensorMap* km, CUtensorMap* vm, bool tc) {
     const int64_t rows = int64_t(c->num_blocks) * 16;
     const int D = c->head_dim, H = c->num_kv_heads;
@@ -134,11 +152,14 @@ pkv_status cache_maps(const pkv_cache* c, CUtensorMap* km, CUtensorMap* vm, bool
         if (st != PKV_OK) return st;
         return tile_map(vm, c->v, rows, int64_t(H) * D / 2, D / 2, swizzle_for(D / 2));
     }
-    const int box = tc ? 128 : D * 2;
-    const CUtensorMapSwizzle swz = tc ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE;
-    st = tile_map(km, c->k, rows, int64_t(H) * D * 2, box, swz);
+    if (tc) {
+        st = chunk_map(km, c->k, rows, int64_t(H) * D * 2, D);
+        if (st != PKV_OK) return st;
+        return chunk_map(vm, c->v, rows, int64_t(H) * D * 2, D);
+    }
+    st = tile_map(km, c->k, rows, int64_t(H) * D * 2, D * 2, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != PKV_OK) return st;
-    return tile_map(vm, c->v, rows, int64_t(H) * D * 2, box, swz);
+    return tile_map(vm, c->v, rows, int64_t(H) * D * 2, D * 2, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // Shared checks + parameter block of both attention entry points.

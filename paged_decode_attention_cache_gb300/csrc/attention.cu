@@ -198,6 +198,7 @@ struct CcMath {
     static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
                                                  const AttnParams&, int kvh, int pb, uint64_t* bar) {
         // byte-addressed maps, box = one kv head's 16 rows
+        mbar_arrive_expect_tx(bar, TX);
         tma_load_2d(dst, km, kvh * D * 2, pb * kBS, bar);
         tma_load_2d(dst + KT, vm, kvh * D * 2, pb * kBS, bar);
     }
@@ -383,7 +384,7 @@ struct TcMath {
     static constexpr int OFF_KS = OFF_V + align_up(VT, 16);
     static constexpr int OFF_VS = OFF_KS + KS;
     static constexpr int OFF_VZ = OFF_VS + VS;
-    static constexpr int TX = KT + VT + KS + 2 * VS;
+    static constexpr int TX = KT + VT;   // bytes the TMA copies deliver
     static constexpr int STAGE = align_up(OFF_VZ + VS, 1024);
     static constexpr int SCRATCH = 0;
     static_assert(OFF_V % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1 KB alignment");
@@ -397,18 +398,31 @@ struct TcMath {
     static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
                                                  const AttnParams& p, int kvh, int pb, uint64_t* bar) {
         if constexpr (Q8) {
+            // The scales and zeros (KS + 2*VS bytes) travel as 16-byte cp.async
+            // copies tracked by the same barrier: the TMA engine's per-SM rate
+            // of copy operations, not bytes, bounds a 3.4 KB block, so it gets
+            // only the two code tiles.
+            const size_t meta = size_t(pb) * p.num_kv_heads + kvh;
+            const uint8_t* ks = reinterpret_cast<const uint8_t*>(p.k_scale) + meta * KS;
+            const uint8_t* vs = reinterpret_cast<const uint8_t*>(p.v_scale) + meta * VS;
+            const uint8_t* vz = reinterpret_cast<const uint8_t*>(p.v_zero) + meta * VS;
+#pragma unroll
+            for (int c = 0; c < KS; c += 16) cp_async_16(dst + OFF_KS + c, ks + c);
+#pragma unroll
+            for (int c = 0; c < VS; c += 16) {
+                cp_async_16(dst + OFF_VS + c, vs + c);
+                cp_async_16(dst + OFF_VZ + c, vz + c);
+            }
+            cp_async_mbar_arrive(bar);
+            mbar_arrive_expect_tx(bar, TX);
             tma_load_2d(dst, km, kvh * D, pb * kBS, bar);
             tma_load_2d(dst + OFF_V, vm, kvh * (D / 2), pb * kBS, bar);
-            const size_t meta = size_t(pb) * p.num_kv_heads + kvh;
-            bulk_load(dst + OFF_KS, reinterpret_cast<const uint8_t*>(p.k_scale) + meta * KS, KS, bar);
-            bulk_load(dst + OFF_VS, reinterpret_cast<const uint8_t*>(p.v_scale) + meta * VS, VS, bar);
-            bulk_load(dst + OFF_VZ, reinterpret_cast<const uint8_t*>(p.v_zero) + meta * VS, VS, bar);
         } else {
-#pragma unroll
-            for (int b = 0; b < D / 64; ++b) {   // 128-byte boxes (64 dims) with the 128B swizzle
-                tma_load_2d(dst + b * 2048, km, kvh * D * 2 + b * 128, pb * kBS, bar);
-                tma_load_2d(dst + OFF_V + b * 2048, vm, kvh * D * 2 + b * 128, pb * kBS, bar);
-            }
+            // one 3-D box per tile: {128 bytes, 16 rows, D/64 chunks} lands as
+            // D/64 consecutive 2 KB sub-tiles of 128-byte rows, 128B swizzle
+            mbar_arrive_expect_tx(bar, TX);
+            tma_load_3d(dst, km, 0, pb * kBS, kvh * (D / 64), bar);
+            tma_load_3d(dst + OFF_V, vm, 0, pb * kBS, kvh * (D / 64), bar);
         }
     }
 
@@ -868,7 +882,9 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     int* flag = reinterpret_cast<int*>(red + 16);
     float* mw = reinterpret_cast<float*>(flag + 4);                  // [NCW][16]
     float* lw = mw + NCW * kMaxRows;                                  // [NCW][16]
-    float* ob = lw + NCW * kMaxRows;                                  // [NCW][M][D]
+    float* rm = lw + NCW * kMaxRows;                                  // [16] merged row max
+    float* rl = rm + kMaxRows;                                        // [16] merged row sum
+    float* ob = rl + kMaxRows;                                        // [NCW][M][D]
     uint8_t* scratch = reinterpret_cast<uint8_t*>(ob + size_t(NCW) * M * D);   // [NCW][SCRATCH]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -942,7 +958,6 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                         pb = 0;   // load a valid block; the consumer masks it out
                     }
                     poison[st] = bad;
-                    mbar_arrive_expect_tx(&full[st], Math::TX);
                     Math::issue(smem + size_t(st) * Math::STAGE, &k_map, &v_map, p, sg.kvh, pb, &full[st]);
                 }
                 issued += min(grp, n - i0);
@@ -954,6 +969,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 
     // ---------------------------------------------------------------- consumers
     constexpr int CT = NCW * 32;   // consumer threads
+    constexpr int kPer = (kMaxRows * 128 / 4 + CT - 1) / CT;   // float4 outputs per thread, at most
     // balanced mode: sequences with nothing visible still get their zero rows
     if (p.mode == kModeBalanced)
         for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x)
@@ -987,45 +1003,88 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         // ------------------------------------------------ merge the warps' states for this segment
         mth.store(ob + size_t(warp) * M * D, mw + warp * kMaxRows, lw + warp * kMaxRows, M, lane);
         named_barrier_sync(1, CT);
+        // per row: the segment max, each warp's weight 2^(m_w - max) (written over m_w) and the sum
+        if (tid < M) {
+            float Mx = -INFINITY;
+#pragma unroll
+            for (int w2 = 0; w2 < NCW; ++w2) Mx = fmaxf(Mx, mw[w2 * kMaxRows + tid]);
+            float L = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < NCW; ++w2) {
+                const float mm = mw[w2 * kMaxRows + tid];
+                const float f = (mm == -INFINITY) ? 0.f : exp2f(mm - Mx);
+                mw[w2 * kMaxRows + tid] = f;
+                L = fmaf(lw[w2 * kMaxRows + tid], f, L);
+            }
+            rm[tid] = Mx;
+            rl[tid] = L;
+        }
+        named_barrier_sync(1, CT);
+        // Every shared-memory read of the merge comes before the first global
+        // store: a store can wait behind this SM's queue of TMA reads, and a
+        // later shared load issued behind it would wait as long.
+        const int n4 = (M * D) >> 2;
+        float4 res[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i4 = tid + k * CT;
+            float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i4 < n4) {
+                const int m = (i4 << 2) / D;
+#pragma unroll
+                for (int w2 = 0; w2 < NCW; ++w2) {
+                    const float f = mw[w2 * kMaxRows + m];
+                    const float4 v = reinterpret_cast<const float4*>(ob + size_t(w2) * M * D)[i4];
+                    O.x = fmaf(v.x, f, O.x);
+                    O.y = fmaf(v.y, f, O.y);
+                    O.z = fmaf(v.z, f, O.z);
+                    O.w = fmaf(v.w, f, O.w);
+                }
+            }
+            res[k] = O;
+        }
+        float resM[kPer], resL[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i4 = tid + k * CT;
+            const int m = i4 < n4 ? (i4 << 2) / D : 0;
+            resM[k] = rm[m];
+            resL[k] = rl[m];
+        }
         const int pair = sg.s * Hkv + sg.kvh;
         const bool piece = (p.mode == kModeBalanced) && !sg.whole;
         // piece slot: unique because (lane_idx + s) grows along a lane's pieces
         const int slot = (lane_idx + sg.s) * Hkv + sg.kvh;
-        for (int idx = tid; idx < M * D; idx += CT) {
-            const int m = idx / D, d = idx - (idx / D) * D;
-            float Mx = -INFINITY;
 #pragma unroll
-            for (int w2 = 0; w2 < NCW; ++w2) Mx = fmaxf(Mx, mw[w2 * kMaxRows + m]);
-            float L = 0.f, O = 0.f;
-            if (Mx != -INFINITY) {
-#pragma unroll
-                for (int w2 = 0; w2 < NCW; ++w2) {
-                    const float mm = mw[w2 * kMaxRows + m];
-                    if (mm != -INFINITY) {
-                        const float f = exp2f(mm - Mx);
-                        L = fmaf(lw[w2 * kMaxRows + m], f, L);
-                        O = fmaf(ob[(size_t(w2) * M + m) * D + d], f, O);
-                    }
-                }
-            }
+        for (int k = 0; k < kPer; ++k) {
+            const int i4 = tid + k * CT;
+            if (i4 >= n4) continue;
+            const int m = (i4 << 2) / D, d = (i4 << 2) - m * D;
+            const float L = resL[k], Mx = resM[k];
             const int h = m / QL, jq = m - (m / QL) * QL;
             const size_t row = size_t(sg.s) * QL + jq;
             const int hg = sg.kvh * G + h;
             if (piece) {
-                p.part_o[(size_t(slot) * kMaxRows + m) * D + d] = O;
-                if (d == 0) {
-                    p.part_ml[(size_t(slot) * kMaxRows + m) * 2] = Mx;
-                    p.part_ml[(size_t(slot) * kMaxRows + m) * 2 + 1] = L;
-                }
-            } else if (p.mode == kModeSplit) {
-                const size_t pi = (row * H + hg) * p.max_partitions + sg.part;
-                p.tmp_out[pi * D + d] = (L > 0.f) ? O / L : 0.f;
-                if (d == 0) {
-                    p.max_logits[pi] = (L > 0.f) ? Mx * kLn2 : -INFINITY;
-                    p.exp_sums[pi] = L;
-                }
+                reinterpret_cast<float4*>(p.part_o + (size_t(slot) * kMaxRows + m) * D)[d >> 2] = res[k];
+                if (d == 0)
+                    reinterpret_cast<float2*>(p.part_ml)[size_t(slot) * kMaxRows + m] = make_float2(Mx, L);
             } else {
-                store_out(p.out, p.out_dtype, (row * H + hg) * D + d, (L > 0.f) ? O / L : 0.f);
+                // a row whose sum is not positive (no visible token, or a NaN read
+                // from a poisoned slot) is written as zeros
+                const bool live = L > 0.f;
+                const float inv = live ? 1.f / L : 0.f;
+                const float4 o = live ? make_float4(res[k].x * inv, res[k].y * inv, res[k].z * inv, res[k].w * inv)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (p.mode == kModeSplit) {
+                    const size_t pi = (row * H + hg) * p.max_partitions + sg.part;
+                    reinterpret_cast<float4*>(p.tmp_out + pi * D)[d >> 2] = o;
+                    if (d == 0) {
+                        p.max_logits[pi] = (L > 0.f) ? Mx * kLn2 : -INFINITY;
+                        p.exp_sums[pi] = L;
+                    }
+                } else {
+                    store_out4(p.out, p.out_dtype, (row * H + hg) * D + d, o);
+                }
             }
         }
         if (piece) {
@@ -1044,7 +1103,6 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 // stage every piece's (max, sum) of every row, then the row's weights
                 float* pm = ob;                    // [np][M] maxima, then weights
                 float* pw = ob + np * M;           // [np][M] sums
-                float* rl = pw + np * M;           // [M] combined sums
                 for (int t = tid; t < np * M; t += CT) {
                     const int c = c_lo + t / M, m = t - (t / M) * M;
                     const size_t sl = size_t((c + sg.s) * Hkv + sg.kvh) * kMaxRows + m;
@@ -1068,25 +1126,51 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                     rl[m] = L;
                 }
                 named_barrier_sync(1, CT);
-                for (int idx = tid; idx < M * D; idx += CT) {
-                    const int m = idx / D, d = idx - (idx / D) * D;
-                    float O = 0.f;
-                    int c = 0;
-                    for (; c + 4 <= np; c += 4) {   // four independent loads in flight
-                        float v[4];
+                // all of a thread's loads of four pieces are in flight together
+                float4 acc[kPer];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            v[u] = __ldcg(&p.part_o[(size_t((c_lo + c + u + sg.s) * Hkv + sg.kvh) * kMaxRows + m) * D + d]);
+                for (int k = 0; k < kPer; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int c = 0; c < np; c += 4) {
+                    float4 v[kPer][4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u) O = fmaf(pm[(c + u) * M + m], v[u], O);
+                    for (int k = 0; k < kPer; ++k) {
+                        const int i4 = tid + k * CT;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            v[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (i4 < n4 && c + u < np) {
+                                const size_t sl = size_t((c_lo + c + u + sg.s) * Hkv + sg.kvh) * kMaxRows;
+                                v[k][u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * D) + i4);
+                            }
+                        }
                     }
-                    for (; c < np; ++c)
-                        O = fmaf(pm[c * M + m],
-                                 __ldcg(&p.part_o[(size_t((c_lo + c + sg.s) * Hkv + sg.kvh) * kMaxRows + m) * D + d]), O);
+#pragma unroll
+                    for (int k = 0; k < kPer; ++k) {
+                        const int i4 = tid + k * CT;
+                        if (i4 >= n4) continue;
+                        const int m = (i4 << 2) / D;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const float f = (c + u < np) ? pm[(c + u) * M + m] : 0.f;
+                            acc[k].x = fmaf(f, v[k][u].x, acc[k].x);
+                            acc[k].y = fmaf(f, v[k][u].y, acc[k].y);
+                            acc[k].z = fmaf(f, v[k][u].z, acc[k].z);
+                            acc[k].w = fmaf(f, v[k][u].w, acc[k].w);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int i4 = tid + k * CT;
+                    if (i4 >= n4) continue;
+                    const int m = (i4 << 2) / D, d = (i4 << 2) - m * D;
                     const float L = rl[m];
+                    const bool live = L > 0.f;
+                    const float inv = live ? 1.f / L : 0.f;
                     const int h = m / QL, jq = m - (m / QL) * QL;
-                    store_out(p.out, p.out_dtype, ((size_t(sg.s) * QL + jq) * H + sg.kvh * G + h) * D + d,
-                              (L > 0.f) ? O / L : 0.f);
+                    store_out4(p.out, p.out_dtype, ((size_t(sg.s) * QL + jq) * H + sg.kvh * G + h) * D + d,
+                               live ? make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f));
                 }
                 if (tid == 0) p.counters[pair] = 0;   // ready for the next launch
             }
@@ -1098,7 +1182,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 template <class Math>
 int smem_bytes(int stages, int M, int D) {
     constexpr int NCW = Math::NCW;
-    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + 16 * 8 + 16 + 2 * NCW * kMaxRows * 4 +
+    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + 16 * 8 + 16 + (2 * NCW + 2) * kMaxRows * 4 +
            NCW * M * D * 4 + NCW * Math::SCRATCH + 1024 + 64;
 }
 

@@ -1,6 +1,6 @@
 // pkv_device.cuh -- device-side building blocks shared by the sm_103a kernels:
 // mbarrier pipeline primitives with bounded waits, TMA tile loads, 1-D bulk
-// copies, 16-bit float unpacking and the device error word.
+// copies, 16-byte cp.async, 16-bit float unpacking and the device error word.
 #pragma once
 
 #include <cuda.h>
@@ -93,6 +93,29 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// 3-D tiled TMA load (coordinates innermost first), completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int32_t x, int32_t y, int32_t z,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// 16-byte global -> shared copy through the load/store path (not the TMA engine).
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+// Makes the current phase of `bar` also wait for every cp.async this thread has
+// issued so far: the pending arrival count goes up by one now and comes back
+// down when those copies have landed.  Call it before this thread's own arrive
+// on the phase, so the phase cannot complete in between.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
     asm volatile(
@@ -146,6 +169,25 @@ __device__ __forceinline__ void store_out(void* out, int dtype, size_t i, float 
         reinterpret_cast<__half*>(out)[i] = __float2half_rn(v);
     else
         reinterpret_cast<float*>(out)[i] = v;
+}
+
+// Four consecutive outputs from element i (a multiple of 4): one 16-byte or 8-byte store.
+__device__ __forceinline__ void store_out4(void* out, int dtype, size_t i, float4 v) {
+    if (dtype == PKV_F32) {
+        reinterpret_cast<float4*>(out)[i >> 2] = v;
+    } else if (dtype == PKV_BF16) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        uint2 w;
+        memcpy(&w.x, &a, 4);
+        memcpy(&w.y, &b, 4);
+        reinterpret_cast<uint2*>(out)[i >> 2] = w;
+    } else {
+        const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        uint2 w;
+        memcpy(&w.x, &a, 4);
+        memcpy(&w.y, &b, 4);
+        reinterpret_cast<uint2*>(out)[i >> 2] = w;
+    }
 }
 
 __device__ __forceinline__ float load_q(const void* q, int dtype, size_t i) {
