@@ -5,11 +5,24 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
 #include "pkv.h"
 #include "pkv_internal.h"
+
+namespace pkv {
+
+bool pdl_enabled() {
+    static const bool on = [] {
+        const char* v = std::getenv("PKV_PDL");
+        return !(v && v[0] == '0' && v[1] == '\0');
+    }();
+    return on;
+}
+
+}  // namespace pkv
 
 namespace {
 
@@ -364,7 +377,8 @@ pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const vo
     p.partition_blocks = seqs->max_blocks_per_seq;
     p.max_partitions = 1;
     p.mode = pkv::kModeBalanced;
-    p.min_chunk = 8;
+    p.min_chunk = pkv::kMinChunk;
+    p.seg_cost = pkv::kSegCost;
     return attn_launch(p, cache, gqa, stream);
 }
 
@@ -455,7 +469,8 @@ pkv_status pkv_paged_attention_balanced_noalloc(void* out, pkv_dtype out_dtype, 
     p.partition_blocks = seqs->max_blocks_per_seq;
     p.max_partitions = 1;
     p.mode = pkv::kModeBalanced;
-    p.min_chunk = 8;
+    p.min_chunk = pkv::kMinChunk;
+    p.seg_cost = pkv::kSegCost;
     return attn_launch(p, cache, gqa, stream);
 }
 

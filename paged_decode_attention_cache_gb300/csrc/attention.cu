@@ -692,6 +692,7 @@ __device__ __forceinline__ long long seq_units(const AttnParams& p, int nb) {
 struct Seg {
     int s, kvh, b0, b1, nb, ctx, part;
     long long pair_start;   // balanced: the sequence's first unit (block) in the lane's list
+    long long cost_base;    // balanced: unit u of this pair sits at cost position u + cost_base
     bool whole;             // the segment is the whole pair
 };
 
@@ -704,6 +705,7 @@ struct SegIter {
     long long start;     // its first unit
     long long n;         // its units
     int nb, ctx;
+    int r;               // non-empty sequences before s in the lane's list
 
     __device__ __forceinline__ void load_seq(const AttnParams& p, int s_, long long start_, int known_ctx = -1) {
         s = s_;
@@ -730,11 +732,15 @@ struct SegIter {
             g.b1 = g.nb;
             g.part = 0;
             g.pair_start = 0;
+            g.cost_base = 0;
             g.whole = true;
             u += 1;
             return true;
         }
-        while (s < p.num_seqs && u >= start + n) load_seq(p, s + 1, start + n);
+        while (s < p.num_seqs && u >= start + n) {
+            r += (n > 0);
+            load_seq(p, s + 1, start + n);
+        }
         if (s >= p.num_seqs) {
             u = u1;
             return false;
@@ -750,6 +756,7 @@ struct SegIter {
             g.b1 = int(k1);
             g.part = 0;
             g.pair_start = start;
+            g.cost_base = (long long)p.seg_cost * (r + 1);
             g.whole = (k == 0 && k1 == n);
             u += k1 - k;
         } else {
@@ -757,6 +764,7 @@ struct SegIter {
             g.b0 = int(k) * p.partition_blocks;
             g.b1 = min(nb, g.b0 + p.partition_blocks);
             g.pair_start = 0;
+            g.cost_base = 0;
             g.whole = false;
             u += 1;
         }
@@ -764,101 +772,101 @@ struct SegIter {
     }
 };
 
-// Block-wide search for the sequence holding unit T: sets *s_out (num_seqs if
-// none) and *start_out (its first unit).  Used when the batch has more
-// sequences than the block has threads.
-__device__ void cta_locate(const AttnParams& p, long long T, long long* red, int* s_out, long long* start_out) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    long long base = 0;
-    for (int r0 = 0; r0 < p.num_seqs; r0 += blockDim.x) {
-        const int s = r0 + threadIdx.x;
-        const long long u = (s < p.num_seqs) ? seq_units(p, (seq_ctx(p, s) + kBS - 1) / kBS) : 0;
-        long long incl = u;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) red[warp] = incl;
-        __syncthreads();
-        long long before = 0, total = 0;
-        for (int w = 0; w < nw; ++w) {
-            if (w < warp) before += red[w];
-            total += red[w];
-        }
-        const long long hi = base + before + incl, lo = hi - u;
-        if (u > 0 && lo <= T && T < hi) {
-            *s_out = s;
-            *start_out = lo;
-        }
-        base += total;
-        __syncthreads();
-    }
-}
-
-// Block-wide plan of a split / balanced CTA: total units of the lane's list,
-// this CTA's range [u0, u1) and the sequence holding u0 (with its first unit
-// and context).  One pass over context_lens when the batch fits the block.
+// Block-wide plan of a split / balanced CTA.  The lane's list holds every
+// sequence's units in order.  Balanced mode charges each non-empty sequence
+// seg_cost virtual units ahead of its first block (the merge and combine of one
+// more segment), then cuts the list's total cost into nlanes equal ranges, so a
+// CTA whose range starts a sequence is given fewer blocks.  Unit u of sequence s
+// sits at cost position u + seg_cost * (r_s + 1), r_s = non-empty sequences
+// before s; CTA k serves cost range [k * chunk, (k + 1) * chunk).
 struct Plan {
     long long u0, u1, chunk, start0;
-    int s0, ctx0;
+    int s0, ctx0, r0;
 };
+
+struct SeqPos {
+    int s, ctx;
+    long long u, U, C;   // units, first unit, first cost position
+};
+
+// One round of nthr sequences from r0: a block-wide scan of (cost << 32 | units)
+// gives this thread's sequence its first unit and cost position.
+__device__ __forceinline__ SeqPos plan_round(const AttnParams& p, int r0, long long* red,
+                                             unsigned long long& base) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    SeqPos sp;
+    sp.s = r0 + threadIdx.x;
+    sp.ctx = sp.s < p.num_seqs ? seq_ctx(p, sp.s) : 0;
+    sp.u = sp.s < p.num_seqs ? seq_units(p, (sp.ctx + kBS - 1) / kBS) : 0;
+    const unsigned long long v =
+        sp.u > 0 ? ((unsigned long long)(sp.u + p.seg_cost) << 32) | (unsigned long long)sp.u : 0ull;
+    unsigned long long incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    if (lane == 31) red[warp] = (long long)incl;
+    __syncthreads();
+    unsigned long long before = 0, total = 0;
+    for (int w = 0; w < nw; ++w) {
+        if (w < warp) before += (unsigned long long)red[w];
+        total += (unsigned long long)red[w];
+    }
+    const unsigned long long excl = base + before + incl - v;
+    sp.U = (long long)(excl & 0xffffffffull);
+    sp.C = (long long)(excl >> 32);
+    base += total;
+    __syncthreads();
+    return sp;
+}
+
+// Where cost positions X0 (this CTA's start) and X1 (its end) fall, if in sp.
+__device__ __forceinline__ void plan_resolve(const AttnParams& p, const SeqPos& sp, long long X0, long long X1,
+                                             long long* red, int* flag) {
+    if (sp.u <= 0) return;
+    const long long sc = p.seg_cost, c_end = sp.C + sc + sp.u;
+    if (sp.C <= X0 && X0 < c_end) {
+        flag[0] = sp.s;
+        flag[2] = sp.ctx;
+        flag[3] = sc > 0 ? int((sp.C - sp.U) / sc) : 0;
+        red[15] = sp.U;
+        red[14] = sp.U + max(0ll, X0 - sp.C - sc);
+    }
+    if (sp.C <= X1 && X1 < c_end) red[13] = sp.U + max(0ll, X1 - sp.C - sc);
+}
 
 __device__ void cta_plan(const AttnParams& p, int lane_idx, int nlanes, long long* red, int* flag, Plan& pl) {
     const int B = p.num_seqs, nthr = blockDim.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = nthr >> 5;
+    unsigned long long base = 0;
+    SeqPos mine{};
+    for (int r0 = 0; r0 < B; r0 += nthr) mine = plan_round(p, r0, red, base);
+    const long long total_u = (long long)(base & 0xffffffffull), total_c = (long long)(base >> 32);
+    long long chunk = (total_c + nlanes - 1) / nlanes;
+    if (p.mode == kModeBalanced && chunk < p.min_chunk + p.seg_cost) chunk = p.min_chunk + p.seg_cost;
+    const long long X0 = lane_idx * chunk, X1 = X0 + chunk;
     if (threadIdx.x == 0) {
-        flag[0] = B;       // s0
-        flag[2] = 0;       // ctx0 (-1: reload)
-        red[15] = 0;       // start0
-    }
-    long long base = 0, my_lo = 0, my_u = 0;
-    int my_s = B, my_ctx = 0;
-    for (int r0 = 0; r0 < B; r0 += nthr) {
-        const int s = r0 + threadIdx.x;
-        const int ctx = s < B ? seq_ctx(p, s) : 0;
-        const long long u = s < B ? seq_units(p, (ctx + kBS - 1) / kBS) : 0;
-        long long incl = u;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) red[warp] = incl;
-        __syncthreads();
-        long long before = 0, total = 0;
-        for (int w = 0; w < nw; ++w) {
-            if (w < warp) before += red[w];
-            total += red[w];
-        }
-        my_lo = base + before + incl - u;
-        my_u = u;
-        my_s = s;
-        my_ctx = ctx;
-        base += total;
-        __syncthreads();
-    }
-    const long long total = base;
-    long long chunk = (total + nlanes - 1) / nlanes;
-    if (p.mode == kModeBalanced && chunk < p.min_chunk) chunk = p.min_chunk;
-    pl.chunk = chunk;
-    pl.u0 = lane_idx * chunk;
-    pl.u1 = pl.u0 + chunk < total ? pl.u0 + chunk : total;
-    if (pl.u0 < pl.u1) {
-        if (B <= nthr) {
-            if (my_u > 0 && my_lo <= pl.u0 && pl.u0 < my_lo + my_u) {
-                flag[0] = my_s;
-                flag[2] = my_ctx;
-                red[15] = my_lo;
-            }
-        } else {
-            if (threadIdx.x == 0) flag[2] = -1;
-            cta_locate(p, pl.u0, red + 0, flag, &red[15]);
-        }
+        flag[0] = B;         // s0
+        flag[2] = 0;         // ctx0
+        flag[3] = 0;         // r0
+        red[15] = 0;         // start0
+        red[14] = total_u;   // u0 (X0 past the end: empty range)
+        red[13] = total_u;   // u1
     }
     __syncthreads();
+    if (B <= nthr) {
+        plan_resolve(p, mine, X0, X1, red, flag);
+    } else {
+        base = 0;
+        for (int r0 = 0; r0 < B; r0 += nthr) plan_resolve(p, plan_round(p, r0, red, base), X0, X1, red, flag);
+    }
+    __syncthreads();
+    pl.chunk = chunk;
+    pl.u0 = red[14];
+    pl.u1 = red[13];
     pl.s0 = flag[0];
     pl.ctx0 = flag[2];
+    pl.r0 = flag[3];
     pl.start0 = red[15];
 }
 
@@ -911,20 +919,23 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         pl.u1 = pl.u0 + pl.chunk < total ? pl.u0 + pl.chunk : total;
         pl.s0 = 0;
         pl.ctx0 = -1;
+        pl.r0 = 0;
         pl.start0 = 0;
         __syncthreads();
     } else {
         cta_plan(p, lane_idx, nlanes, red, flag, pl);
     }
     const long long chunk = pl.chunk;
-    // context longer than its table: flagged once per sequence
-    for (int s = blockIdx.x * blockDim.x + tid; s < p.num_seqs; s += gridDim.x * blockDim.x)
-        if (p.context_lens[s] > p.max_blocks * kBS) flag_error(p.err, PKV_DEVERR_CAPACITY);
+    // Everything above read only the launch's inputs (context lengths), which no
+    // kernel of this library writes; what follows waits for the previous kernel
+    // of the stream before it reads the cache or writes anything.
+    if (tid == 0) grid_dep_launch();
 
     SegIter it;
     it.u = pl.u0;
     it.u1 = pl.u0 < pl.u1 ? pl.u1 : pl.u0;
     it.kvh = lane_kvh;
+    it.r = pl.r0;
     if (p.mode != kModeSingle) it.load_seq(p, pl.s0, pl.start0, pl.ctx0);
 
     if (warp == NCW) {
@@ -940,13 +951,18 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         // stage touched in a pass was issued by an earlier pass.
         const int grp = S < 16 ? S : 16;
         int issued = 0;   // blocks issued by this CTA
+        bool waited = false;
         Seg sg;
         while (it.next(p, sg)) {
             const int32_t* bt = p.block_tables + size_t(sg.s) * p.max_blocks;
             const int n = sg.b1 - sg.b0;
             for (int i0 = 0; i0 < n; i0 += grp) {
                 if (lane < grp && i0 + lane < n) {
-                    int pb = bt[sg.b0 + i0 + lane];
+                    int pb = bt[sg.b0 + i0 + lane];   // block tables: an input, read before the wait
+                    if (!waited) {
+                        grid_dep_wait();
+                        waited = true;
+                    }
                     const int j = issued + lane;
                     const int st = j % S;
                     const int use = j / S;
@@ -969,6 +985,10 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 
     // ---------------------------------------------------------------- consumers
     constexpr int CT = NCW * 32;   // consumer threads
+    grid_dep_wait();
+    // context longer than its table: flagged once per sequence
+    for (int s = blockIdx.x * CT + tid; s < p.num_seqs; s += gridDim.x * CT)
+        if (p.context_lens[s] > p.max_blocks * kBS) flag_error(p.err, PKV_DEVERR_CAPACITY);
     constexpr int kPer = (kMaxRows * 128 / 4 + CT - 1) / CT;   // float4 outputs per thread, at most
     // balanced mode: sequences with nothing visible still get their zero rows
     if (p.mode == kModeBalanced)
@@ -1091,7 +1111,8 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             // the last piece of a pair to finish combines all of them (no waiting)
             __threadfence();
             named_barrier_sync(1, CT);
-            const int c_lo = int(sg.pair_start / chunk), c_hi = int((sg.pair_start + sg.nb - 1) / chunk);
+            const int c_lo = int((sg.pair_start + sg.cost_base) / chunk),
+                      c_hi = int((sg.pair_start + sg.nb - 1 + sg.cost_base) / chunk);
             const int np = c_hi - c_lo + 1;
             if (tid == 0) {
                 const int prev = atomicAdd(&p.counters[pair], 1);
@@ -1100,63 +1121,55 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             named_barrier_sync(1, CT);
             if (flag[1]) {
                 __threadfence();
-                // stage every piece's (max, sum) of every row, then the row's weights
-                float* pm = ob;                    // [np][M] maxima, then weights
-                float* pw = ob + np * M;           // [np][M] sums
-                for (int t = tid; t < np * M; t += CT) {
-                    const int c = c_lo + t / M, m = t - (t / M) * M;
-                    const size_t sl = size_t((c + sg.s) * Hkv + sg.kvh) * kMaxRows + m;
-                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl);
-                    pm[t] = ml.x;
-                    pw[t] = ml.y;
-                }
-                named_barrier_sync(1, CT);
-                // pieces hold unnormalised sums relative to their own max m_c:
-                // O = sum_c 2^(m_c - M) O_c, L = sum_c 2^(m_c - M) l_c
-                for (int m = tid; m < M; m += CT) {
-                    float Mx = -INFINITY;
-                    for (int c = 0; c < np; ++c)
-                        if (pw[c * M + m] > 0.f) Mx = fmaxf(Mx, pm[c * M + m]);
-                    float L = 0.f;
-                    for (int c = 0; c < np; ++c) {
-                        const float f = (pw[c * M + m] > 0.f) ? exp2f(pm[c * M + m] - Mx) : 0.f;
-                        pm[c * M + m] = f;
-                        L = fmaf(pw[c * M + m], f, L);
-                    }
-                    rl[m] = L;
-                }
-                named_barrier_sync(1, CT);
-                // all of a thread's loads of four pieces are in flight together
+                // Pieces hold unnormalised sums relative to their own max m_c:
+                // O = sum_c 2^(m_c - M) O_c, L = sum_c 2^(m_c - M) l_c.  Four pieces
+                // at a time, each with its (m, l) and its slice of O loaded in the
+                // same round trip, folded in by an online rescale.
                 float4 acc[kPer];
+                float Mr[kPer], Lr[kPer];
 #pragma unroll
-                for (int k = 0; k < kPer; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int k = 0; k < kPer; ++k) {
+                    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    Mr[k] = -INFINITY;
+                    Lr[k] = 0.f;
+                }
                 for (int c = 0; c < np; c += 4) {
+                    float2 ml[kPer][4];
                     float4 v[kPer][4];
 #pragma unroll
                     for (int k = 0; k < kPer; ++k) {
                         const int i4 = tid + k * CT;
+                        const int m = i4 < n4 ? (i4 << 2) / D : 0;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
+                            ml[k][u] = make_float2(-INFINITY, 0.f);
                             v[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
                             if (i4 < n4 && c + u < np) {
                                 const size_t sl = size_t((c_lo + c + u + sg.s) * Hkv + sg.kvh) * kMaxRows;
+                                ml[k][u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl + m);
                                 v[k][u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * D) + i4);
                             }
                         }
                     }
 #pragma unroll
                     for (int k = 0; k < kPer; ++k) {
-                        const int i4 = tid + k * CT;
-                        if (i4 >= n4) continue;
-                        const int m = (i4 << 2) / D;
+                        float Mn = Mr[k];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            if (ml[k][u].y > 0.f) Mn = fmaxf(Mn, ml[k][u].x);
+                        const float a = (Mr[k] == -INFINITY) ? 0.f : exp2f(Mr[k] - Mn);
+                        acc[k].x *= a; acc[k].y *= a; acc[k].z *= a; acc[k].w *= a;
+                        Lr[k] *= a;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const float f = (c + u < np) ? pm[(c + u) * M + m] : 0.f;
+                            const float f = (ml[k][u].y > 0.f) ? exp2f(ml[k][u].x - Mn) : 0.f;
                             acc[k].x = fmaf(f, v[k][u].x, acc[k].x);
                             acc[k].y = fmaf(f, v[k][u].y, acc[k].y);
                             acc[k].z = fmaf(f, v[k][u].z, acc[k].z);
                             acc[k].w = fmaf(f, v[k][u].w, acc[k].w);
+                            Lr[k] = fmaf(f, ml[k][u].y, Lr[k]);
                         }
+                        Mr[k] = Mn;
                     }
                 }
 #pragma unroll
@@ -1164,7 +1177,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                     const int i4 = tid + k * CT;
                     if (i4 >= n4) continue;
                     const int m = (i4 << 2) / D, d = (i4 << 2) - m * D;
-                    const float L = rl[m];
+                    const float L = Lr[k];
                     const bool live = L > 0.f;
                     const float inv = live ? 1.f / L : 0.f;
                     const int h = m / QL, jq = m - (m / QL) * QL;
@@ -1223,8 +1236,8 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
         if (lane_units < L) L = int(lane_units < 1 ? 1 : lane_units);
         grid = L * p.num_kv_heads;
     }
-    attention_kernel<Math><<<grid, (Math::NCW + 1) * 32, smem, stream>>>(km, vm, p);
-    return cudaGetLastError();
+    return launch_kernel(attention_kernel<Math>, dim3(grid), dim3((Math::NCW + 1) * 32), size_t(smem), stream, km, vm,
+                         p);
 }
 
 template <typename T, int D>

@@ -21,6 +21,8 @@ constexpr int kThreads = 256;
 // all kv heads is contiguous in both the source [T, Hkv, D] and the cache
 // [NB, 16, Hkv, D], so each token is `chunks` 16-byte chunks copied verbatim.
 __global__ void __launch_bounds__(kThreads) reshape_and_cache_kernel(CacheWriteParams p, int chunks) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int64_t total = int64_t(p.num_tokens) * chunks;
     const int64_t pool = int64_t(p.num_blocks) * kBlockSize;
     for (int64_t i = blockIdx.x * int64_t(kThreads) + threadIdx.x; i < total;
@@ -47,6 +49,8 @@ __global__ void __launch_bounds__(kThreads) reshape_and_cache_kernel(CacheWriteP
 //  gather_kv_cache names the read back to contiguous storage.]  CTA (b, s)
 // copies logical block b of sequence s.
 __global__ void __launch_bounds__(kThreads) gather_kernel(GatherParams p, int chunks) {
+    grid_dep_wait();
+    grid_dep_launch();
     const int s = blockIdx.y, b = blockIdx.x;
     int ctx = p.context_lens[s];
     const int cap = p.max_blocks * kBlockSize;
@@ -84,6 +88,8 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherParams p, int ch
 // conversion of scales to fp16 before they are used.
 template <typename Src, int D>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(CacheWriteParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     constexpr int E = D / 32;            // values per lane
     constexpr int kGroup = 32;           // V group size along head_dim
     constexpr int NG = D / kGroup;       // groups per row
@@ -179,15 +185,14 @@ int grid_for(int64_t work, int per_cta) {
 
 cudaError_t launch_reshape_and_cache(const CacheWriteParams& p, int elem_bytes, cudaStream_t stream) {
     const int chunks = p.num_kv_heads * p.head_dim * elem_bytes / 16;
-    reshape_and_cache_kernel<<<grid_for(int64_t(p.num_tokens) * chunks, kThreads), kThreads, 0, stream>>>(p, chunks);
-    return cudaGetLastError();
+    return launch_kernel(reshape_and_cache_kernel, dim3(grid_for(int64_t(p.num_tokens) * chunks, kThreads)),
+                         dim3(kThreads), 0, stream, p, chunks);
 }
 
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, cudaStream_t stream) {
     const int chunks = p.num_kv_heads * p.head_dim * elem_bytes / 16;
     dim3 grid(p.max_blocks, p.num_seqs);
-    gather_kernel<<<grid, kThreads, 0, stream>>>(p, chunks);
-    return cudaGetLastError();
+    return launch_kernel(gather_kernel, grid, dim3(kThreads), 0, stream, p, chunks);
 }
 
 cudaError_t launch_quantize_kv(const CacheWriteParams& p, cudaStream_t stream) {
@@ -196,18 +201,9 @@ cudaError_t launch_quantize_kv(const CacheWriteParams& p, cudaStream_t stream) {
     if (g64 > 0x7fffffff) return cudaErrorInvalidValue;
     const int grid = int(g64 < 1 ? 1 : g64);
     const bool bf = p.src_dtype == PKV_BF16;
-    if (p.head_dim == 128) {
-        if (bf)
-            quantize_kernel<__nv_bfloat16, 128><<<grid, kThreads, 0, stream>>>(p);
-        else
-            quantize_kernel<__half, 128><<<grid, kThreads, 0, stream>>>(p);
-    } else {
-        if (bf)
-            quantize_kernel<__nv_bfloat16, 64><<<grid, kThreads, 0, stream>>>(p);
-        else
-            quantize_kernel<__half, 64><<<grid, kThreads, 0, stream>>>(p);
-    }
-    return cudaGetLastError();
+    auto* k = p.head_dim == 128 ? (bf ? quantize_kernel<__nv_bfloat16, 128> : quantize_kernel<__half, 128>)
+                                : (bf ? quantize_kernel<__nv_bfloat16, 64> : quantize_kernel<__half, 64>);
+    return launch_kernel(k, dim3(grid), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace pkv

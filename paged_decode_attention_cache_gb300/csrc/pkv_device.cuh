@@ -80,6 +80,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     }
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+
+// Wait until every grid this launch programmatically depends on has completed
+// and its writes are visible.  Returns at once for a launch without such a
+// dependency.  Every kernel here calls it before its first global write and
+// before reading anything a kernel of this library writes.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel of the stream be scheduled now; it still runs its own
+// grid_dep_wait() before touching memory this grid writes.
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ---------------------------------------------------------------- TMA / bulk copies
 
 // 2-D tiled TMA load of one box into shared memory, completing on `bar`.

@@ -10,6 +10,28 @@
 
 namespace pkv {
 
+// Kernel launch with programmatic stream serialisation: the kernel may start
+// while the previous kernel of the stream is finishing, and waits on the device
+// (griddepcontrol.wait) before it touches memory that kernel could write.
+// PKV_PDL=0 in the environment launches without the attribute.
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // Everything the attention kernels read besides the two tensor maps.
 struct AttnParams {
     // outputs: exactly one of {out} or {tmp_out, max_logits, exp_sums} is set
@@ -43,6 +65,7 @@ struct AttnParams {
     int32_t mode;       // kModeSingle / kModeSplit / kModeBalanced
     int32_t stages;     // shared-memory ring depth (a multiple of the consumer warps)
     int32_t min_chunk;  // balanced: fewest 16-token blocks a CTA is given
+    int32_t seg_cost;   // balanced: blocks' worth of time one more segment costs a CTA
     float* part_o;      // balanced workspace: [slots, 16, head_dim] unnormalised partial outputs
     float* part_ml;     // [slots, 16, 2] (max, sum) in base-2 units
     int32_t* counters;  // [num_seqs * num_kv_heads] pieces finished per (sequence, kv head)
@@ -52,6 +75,11 @@ constexpr int kModeSingle = 0;
 constexpr int kModeSplit = 1;
 constexpr int kModeBalanced = 2;
 constexpr int kMaxGrid = 1024;  // CTAs of a persistent launch (bounds the balanced workspace)
+// Balanced schedule: a CTA gets at least kMinChunk blocks, and starting one more
+// (sequence, kv head) segment is charged as kSegCost blocks (its merge and
+// combine take about as long as streaming that many blocks).
+constexpr int kMinChunk = 8;
+constexpr int kSegCost = 24;
 
 // Persistent attention kernel (attention.cu): one CTA per SM at most, the
 // (sequence, kv head, block) work list split into contiguous ranges.

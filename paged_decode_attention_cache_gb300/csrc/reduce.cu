@@ -24,6 +24,8 @@ constexpr int kMaxStaged = 2048;   // partitions whose weights fit the shared bu
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) lse_reduce_kernel(ReduceParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
     constexpr int CH = D / 4;              // float4 chunks of one row
     constexpr int NGRP = kThreads / CH;    // partition groups (8 for D=128, 16 for D=64)
     __shared__ float w_s[kMaxStaged];
@@ -125,11 +127,8 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream) {
     const int rows = p.num_seqs * p.q_len;
     if (p.num_heads > 65535) return cudaErrorInvalidValue;
     dim3 grid(rows, p.num_heads);
-    if (p.head_dim == 128)
-        lse_reduce_kernel<128><<<grid, kThreads, 0, stream>>>(p);
-    else
-        lse_reduce_kernel<64><<<grid, kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_kernel(p.head_dim == 128 ? lse_reduce_kernel<128> : lse_reduce_kernel<64>, grid, dim3(kThreads), 0,
+                         stream, p);
 }
 
 }  // namespace pkv
