@@ -676,6 +676,310 @@ struct TcMath {
     float scale_log2_;
 };
 
+// ---------------------------------------------------------------- K8/V4 block math, transposed
+
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {   // 8x8 b16 matrix transpose across the warp
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+    __half2 x, y;
+    memcpy(&x, &a, 4);
+    memcpy(&y, &b, 4);
+    const __half2 z = __hmul2(x, y);
+    uint32_t r;
+    memcpy(&r, &z, 4);
+    return r;
+}
+
+// K8/V4 cache (see quantize_kernel).  The query tile of a decode block is only
+// g*q_len rows, so the contraction is turned around: S^T = K Q^T puts the 16
+// tokens on the MMA's M side and up to 8 (NT = 1) or 16 (NT = 2) query columns
+// on N, and O^T = V^T P^T puts 16 head dims on M.  Per 16-token block and 8
+// query columns that is D/16 MMAs for the scores and D/16 for the values,
+// where a 16-row query tile needs twice as many.
+//   K: int8 codes -> exact fp16 integers; the per-token K scale multiplies the
+//      scores.  A thread's four k positions of a k-step are four consecutive
+//      bytes of a row; the query operand uses the same dim order.
+//   V: 4-bit codes -> exact fp16 integers in the A operand (ldmatrix.trans of
+//      16-bit words = 4 dims x 2 tokens).  A 16-byte chunk of a V row is one
+//      32-dim group, and an M tile takes dims {4w+i, 4w+i+2} of one group, so
+//      the per-(token, group) scale goes into the P^T operand (P * s in fp16)
+//      and the zero point into one more MMA, Z^T P^T, added at the end.
+//   P: the S^T accumulator is packed to fp16 and turned into the P^T operand
+//      with movmatrix.
+template <int D, int NT>
+struct TqMath {
+    static constexpr bool kTensor = true;
+    // NT = 1: 11 consumer warps at <= 168 registers; NT = 2: 7 at <= 255
+    static constexpr int NCW = NT == 1 ? 11 : 7;
+    static constexpr int NG = D / 32;      // V groups
+    static constexpr int NKS = D / 16;     // k-steps of the score contraction
+    static constexpr int KT = kBS * D;
+    static constexpr int VT = kBS * D / 2;
+    static constexpr int KS = kBS * 2;
+    static constexpr int VS = kBS * NG * 2;
+    static constexpr int OFF_V = align_up(KT, 1024);
+    static constexpr int OFF_KS = OFF_V + align_up(VT, 16);
+    static constexpr int OFF_VS = OFF_KS + KS;
+    static constexpr int OFF_VZ = OFF_VS + VS;
+    static constexpr int TX = KT + VT;   // bytes the TMA copies deliver
+    static constexpr int STAGE = align_up(OFF_VZ + VS, 1024);
+    static constexpr int SCRATCH = 0;
+    static_assert(OFF_V % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1 KB alignment");
+
+    uint32_t qb[NT][NKS][2];   // Q^T operand: query column g (+8), this thread's dims
+    float o[NT][2 * NG][4];    // O^T accumulators: M tile (group, i) x 8 query columns
+    float cz[NT][4];           // Z^T P^T: rows = groups
+    float m_run[NT][2], l_part[NT][2];   // per query column 2t, 2t+1 (l: this thread's tokens)
+    int lim[NT][2];
+    float scale_log2_;
+
+    static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
+                                                 const AttnParams& p, int kvh, int pb, uint64_t* bar) {
+        const size_t meta = size_t(pb) * p.num_kv_heads + kvh;
+        const uint8_t* ks = reinterpret_cast<const uint8_t*>(p.k_scale) + meta * KS;
+        const uint8_t* vs = reinterpret_cast<const uint8_t*>(p.v_scale) + meta * VS;
+        const uint8_t* vz = reinterpret_cast<const uint8_t*>(p.v_zero) + meta * VS;
+#pragma unroll
+        for (int c = 0; c < KS; c += 16) cp_async_16(dst + OFF_KS + c, ks + c);
+#pragma unroll
+        for (int c = 0; c < VS; c += 16) {
+            cp_async_16(dst + OFF_VS + c, vs + c);
+            cp_async_16(dst + OFF_VZ + c, vz + c);
+        }
+        cp_async_mbar_arrive(bar);
+        mbar_arrive_expect_tx(bar, TX);
+        tma_load_2d(dst, km, kvh * D, pb * kBS, bar);
+        tma_load_2d(dst + OFF_V, vm, kvh * (D / 2), pb * kBS, bar);
+    }
+
+    __device__ __forceinline__ void init(int) {}
+
+    // query column n = head (n / q_len), draft (n % q_len)
+    __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+        const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int n = 8 * nt + g;
+            const bool valid = n < M;
+            const int h = valid ? n / QL : 0, j = valid ? n % QL : 0;
+            const size_t qoff = ((size_t(s) * QL + j) * p.num_heads + kvh * G + h) * D;
+#pragma unroll
+            for (int kk = 0; kk < NKS; ++kk) {
+                uint32_t lo = 0, hi = 0;
+                if (valid) {
+                    const int d0 = t * (D / 4) + 4 * kk;
+                    lo = pack2<false>(load_q(p.q, p.q_dtype, qoff + d0), load_q(p.q, p.q_dtype, qoff + d0 + 1));
+                    hi = pack2<false>(load_q(p.q, p.q_dtype, qoff + d0 + 2), load_q(p.q, p.q_dtype, qoff + d0 + 3));
+                }
+                qb[nt][kk][0] = lo;
+                qb[nt][kk][1] = hi;
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int n2 = 8 * nt + 2 * t + e;
+                lim[nt][e] = n2 < M ? max(0, ctx - QL + n2 % QL + 1) : 0;
+                m_run[nt][e] = -INFINITY;
+                l_part[nt][e] = 0.f;
+            }
+#pragma unroll
+            for (int mt = 0; mt < 2 * NG; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
+            cz[nt][0] = cz[nt][1] = cz[nt][2] = cz[nt][3] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void block(const uint8_t* stg, int pos0, int ntok, uint8_t*, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+        const uint32_t stg_a = smem_addr(stg);
+        // ------------------------------------------------ S^T = K Q^T (rows = tokens g, g+8)
+        uint32_t w[2][NKS];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int row = g + 8 * r;
+#pragma unroll
+            for (int i = 0; i < D / 64; ++i) {
+                const int c = t * (D / 64) + i;
+                const uint4 v = *reinterpret_cast<const uint4*>(stg + row * D + 16 * swz<D>(c, row));
+                w[r][4 * i] = v.x; w[r][4 * i + 1] = v.y; w[r][4 * i + 2] = v.z; w[r][4 * i + 3] = v.w;
+            }
+        }
+        float sc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < NKS; ++kk) {
+            uint32_t a[4];
+            s8x4_to_f16x4(w[0][kk], a[0], a[2]);
+            s8x4_to_f16x4(w[1][kk], a[1], a[3]);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
+        // K scale per token, base-2 softmax scale, causal / context mask
+        const __half* ksh = reinterpret_cast<const __half*>(stg + OFF_KS);
+        const float k0 = __half2float(ksh[g]) * scale_log2_, k1 = __half2float(ksh[g + 8]) * scale_log2_;
+        const int pg = pos0 + g, pg8 = pos0 + g + 8;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            sc[nt][0] = (pg < lim[nt][0]) ? sc[nt][0] * k0 : -INFINITY;
+            sc[nt][1] = (pg < lim[nt][1]) ? sc[nt][1] * k0 : -INFINITY;
+            sc[nt][2] = (pg8 < lim[nt][0]) ? sc[nt][2] * k1 : -INFINITY;
+            sc[nt][3] = (pg8 < lim[nt][1]) ? sc[nt][3] * k1 : -INFINITY;
+        }
+        // ------------------------------------------------ online softmax per query column
+        float alpha[NT][2];
+        bool rescale = false;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float bm = fmaxf(sc[nt][e], sc[nt][2 + e]);
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+                bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+                const float mn = fmaxf(m_run[nt][e], bm);
+                const float mu = (mn == -INFINITY) ? 0.f : mn;
+                alpha[nt][e] = exp2f(m_run[nt][e] - mu);
+                const float p0 = exp2f(sc[nt][e] - mu), p1 = exp2f(sc[nt][2 + e] - mu);
+                sc[nt][e] = p0;
+                sc[nt][2 + e] = p1;
+                l_part[nt][e] = l_part[nt][e] * alpha[nt][e] + (p0 + p1);
+                m_run[nt][e] = mn;
+                rescale |= alpha[nt][e] != 1.f;
+            }
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int mt = 0; mt < 2 * NG; ++mt) {
+                    o[nt][mt][0] *= alpha[nt][0]; o[nt][mt][2] *= alpha[nt][0];
+                    o[nt][mt][1] *= alpha[nt][1]; o[nt][mt][3] *= alpha[nt][1];
+                }
+                cz[nt][0] *= alpha[nt][0];
+                cz[nt][1] *= alpha[nt][1];
+            }
+        }
+        // ------------------------------------------------ P^T operand (tokens 2t.. , query g)
+        uint32_t pb[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            pb[nt][0] = movm_trans(pack2<false>(sc[nt][0], sc[nt][1]));
+            pb[nt][1] = movm_trans(pack2<false>(sc[nt][2], sc[nt][3]));
+        }
+        // per-token V scales / zeros of tokens 2t, 2t+1, 2t+8, 2t+9 (all groups);
+        // rows past the context hold NaN and are zeroed (their P is 0)
+        constexpr int RW = (NG * 2 + 3) / 4;   // 32-bit words per token row
+        uint32_t sr[4][RW], zr[4][RW];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int tk = 2 * t + (i & 1) + 8 * (i >> 1);
+            const uint32_t* sp = reinterpret_cast<const uint32_t*>(stg + OFF_VS + tk * NG * 2);
+            const uint32_t* zp = reinterpret_cast<const uint32_t*>(stg + OFF_VZ + tk * NG * 2);
+#pragma unroll
+            for (int q = 0; q < RW; ++q) {
+                sr[i][q] = sp[q];
+                zr[i][q] = zp[q];
+            }
+            if (tk >= ntok) {
+#pragma unroll
+                for (int q = 0; q < RW; ++q) sr[i][q] = zr[i][q] = 0u;
+            }
+        }
+        // ------------------------------------------------ O^T += V^T (P^T * s), Z^T P^T
+#pragma unroll
+        for (int g0 = 0; g0 < NG; g0 += 2) {
+            const int mi = lane >> 3, r = lane & 7;
+            const int tok = (mi & 1) * 8 + r, c = g0 + (mi >> 1);   // 16-byte chunk = group
+            const uint32_t addr = stg_a + OFF_V + tok * (D / 2) + 16 * swz<D / 2>(c, tok);
+            uint32_t X[4];
+            ldsm_x4_t(addr, X);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int gg = g0 + h;
+                const uint32_t xlo = X[2 * h], xhi = X[2 * h + 1];
+                // {s[token a][gg], s[token b][gg]} pairs for tokens (2t, 2t+1) and (2t+8, 2t+9)
+                const uint32_t sel = (gg & 1) ? 0x7632u : 0x5410u;
+                const uint32_t s01 = __byte_perm(sr[0][gg >> 1], sr[1][gg >> 1], sel);
+                const uint32_t s89 = __byte_perm(sr[2][gg >> 1], sr[3][gg >> 1], sel);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    uint32_t a[4];
+                    a[0] = u4pair_to_f16x2(xlo, i);
+                    a[1] = u4pair_to_f16x2(xlo, i + 2);
+                    a[2] = u4pair_to_f16x2(xhi, i);
+                    a[3] = u4pair_to_f16x2(xhi, i + 2);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_f16(o[nt][2 * gg + i], a, hmul2_u32(pb[nt][0], s01), hmul2_u32(pb[nt][1], s89));
+                }
+            }
+        }
+        {
+            // zero points: A rows = groups (row g of this thread, g < NG), k = tokens
+            const uint32_t sel = (g & 1) ? 0x7632u : 0x5410u;
+            uint32_t z[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) z[i] = (RW > 1 && (g & 2)) ? zr[i][RW - 1] : zr[i][0];
+            uint32_t za[4];
+            za[0] = g < NG ? __byte_perm(z[0], z[1], sel) : 0u;
+            za[1] = 0u;
+            za[2] = g < NG ? __byte_perm(z[2], z[3], sel) : 0u;
+            za[3] = 0u;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(cz[nt], za, pb[nt][0], pb[nt][1]);
+        }
+    }
+
+    // add the zero-point term of each group, then sum l over the 8 token lanes
+    __device__ __forceinline__ void finish(int lane) {
+        const int t = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                const float z0 = __shfl_sync(0xffffffffu, cz[nt][0], gg * 4 + t);
+                const float z1 = __shfl_sync(0xffffffffu, cz[nt][1], gg * 4 + t);
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    o[nt][2 * gg + i][0] += z0; o[nt][2 * gg + i][2] += z0;
+                    o[nt][2 * gg + i][1] += z1; o[nt][2 * gg + i][3] += z1;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float l = l_part[nt][e];
+                l += __shfl_xor_sync(0xffffffffu, l, 4);
+                l += __shfl_xor_sync(0xffffffffu, l, 8);
+                l += __shfl_xor_sync(0xffffffffu, l, 16);
+                l_part[nt][e] = l;
+            }
+        }
+    }
+
+    // unnormalised rows [M][D] and per-row (m, l) of this warp
+    __device__ __forceinline__ void store(float* ob, float* mw, float* lw, int M, int lane) const {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int q = 8 * nt + 2 * t + e;
+                if (q >= M) continue;
+#pragma unroll
+                for (int gg = 0; gg < NG; ++gg)
+                    *reinterpret_cast<float4*>(ob + q * D + 32 * gg + 4 * g) =
+                        make_float4(o[nt][2 * gg][e], o[nt][2 * gg + 1][e], o[nt][2 * gg][2 + e], o[nt][2 * gg + 1][2 + e]);
+                if (g == 0) {
+                    mw[q] = m_run[nt][e];
+                    lw[q] = l_part[nt][e];
+                }
+            }
+    }
+};
+
 // ---------------------------------------------------------------- work list
 
 __device__ __forceinline__ int seq_ctx(const AttnParams& p, int s) {
@@ -1266,9 +1570,14 @@ cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtens
                              cudaStream_t stream) {
     if (attention_uses_tensor_cores(cache_kind, p.q_len)) {
         switch (cache_kind) {
-            case PKV_CACHE_K8V4:
-                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_K8V4, 128>>(p, km, vm, stream)
-                                         : launch_math<TcMath<PKV_CACHE_K8V4, 64>>(p, km, vm, stream);
+            case PKV_CACHE_K8V4: {
+                const bool narrow = (p.num_heads / p.num_kv_heads) * p.q_len <= 8;
+                if (p.head_dim == 128)
+                    return narrow ? launch_math<TqMath<128, 1>>(p, km, vm, stream)
+                                  : launch_math<TqMath<128, 2>>(p, km, vm, stream);
+                return narrow ? launch_math<TqMath<64, 1>>(p, km, vm, stream)
+                              : launch_math<TqMath<64, 2>>(p, km, vm, stream);
+            }
             case PKV_CACHE_BF16:
                 return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_BF16, 128>>(p, km, vm, stream)
                                          : launch_math<TcMath<PKV_CACHE_BF16, 64>>(p, km, vm, stream);
