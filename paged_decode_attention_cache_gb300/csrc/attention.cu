@@ -62,6 +62,11 @@ constexpr int kSmemLimit = 227 * 1024;
 
 constexpr int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
+// Element (m, d) of a per-warp merge buffer [M][D] (floats): 32-byte units of a
+// row are XOR-permuted by the row, so the 8 rows a warp's fragment store
+// touches at once fall in different banks; 16-byte groups stay together.
+__host__ __device__ constexpr int ob_idx(int m, int d, int D) { return m * D + (d ^ ((m & 7) << 3)); }
+
 // ---------------------------------------------------------------- small device helpers
 
 template <int W>
@@ -357,73 +362,45 @@ struct CcMath {
 #pragma unroll
         for (int h = 0; h < G; ++h)
 #pragma unroll
-            for (int e = 0; e < DPL / 2; ++e) reinterpret_cast<float2*>(ob + h * D + lane * DPL)[e] = acc[h][e];
+            for (int e = 0; e < DPL / 2; ++e)
+                *reinterpret_cast<float2*>(ob + ob_idx(h, lane * DPL + 2 * e, D)) = acc[h][e];
     }
 };
 
 // ---------------------------------------------------------------- tensor-core block math
 
+// Multi-token verify blocks on fp16 / bf16 caches: the 16-row query tile (g
+// heads x q_len drafts) against a 16-token block.
 template <int KIND, int D>
 struct TcMath {
     static constexpr bool kTensor = true;
     // 7 consumer warps + the producer: 8 warps, two per SM sub-partition, so a
     // thread may use up to 255 registers (the MMA fragments need ~230)
     static constexpr int NCW = 7;
-    static constexpr bool Q8 = KIND == PKV_CACHE_K8V4;
     static constexpr bool BF = KIND == PKV_CACHE_BF16;
-    static constexpr int NG = D / 32;
     static constexpr int NKS = D / 16;
     static constexpr int NNT = D / 8;
-    static constexpr int KROW = Q8 ? D : 2 * D;
-    static constexpr int VROW = Q8 ? D / 2 : 2 * D;
-    static constexpr int KT = kBS * KROW;
-    static constexpr int VT = kBS * VROW;
-    static constexpr int KS = Q8 ? kBS * 2 : 0;
-    static constexpr int VS = Q8 ? kBS * NG * 2 : 0;
+    static constexpr int KT = kBS * 2 * D;
+    static constexpr int VT = kBS * 2 * D;
     static constexpr int OFF_V = align_up(KT, 1024);
-    static constexpr int OFF_KS = OFF_V + align_up(VT, 16);
-    static constexpr int OFF_VS = OFF_KS + KS;
-    static constexpr int OFF_VZ = OFF_VS + VS;
     static constexpr int TX = KT + VT;   // bytes the TMA copies deliver
-    static constexpr int STAGE = align_up(OFF_VZ + VS, 1024);
+    static constexpr int STAGE = align_up(OFF_V + VT, 1024);
     static constexpr int SCRATCH = 0;
+    static_assert(KIND != PKV_CACHE_K8V4, "K8/V4 runs TqMath");
     static_assert(OFF_V % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1 KB alignment");
 
     uint32_t qa[NKS][4];
     float o[NNT][4];
     float m_run[2], l_run[2];
-    float zacc[2][NG];
     int lim[2];
 
     static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
-                                                 const AttnParams& p, int kvh, int pb, uint64_t* bar) {
-        if constexpr (Q8) {
-            // The scales and zeros (KS + 2*VS bytes) travel as 16-byte cp.async
-            // copies tracked by the same barrier: the TMA engine's per-SM rate
-            // of copy operations, not bytes, bounds a 3.4 KB block, so it gets
-            // only the two code tiles.
-            const size_t meta = size_t(pb) * p.num_kv_heads + kvh;
-            const uint8_t* ks = reinterpret_cast<const uint8_t*>(p.k_scale) + meta * KS;
-            const uint8_t* vs = reinterpret_cast<const uint8_t*>(p.v_scale) + meta * VS;
-            const uint8_t* vz = reinterpret_cast<const uint8_t*>(p.v_zero) + meta * VS;
-#pragma unroll
-            for (int c = 0; c < KS; c += 16) cp_async_16(dst + OFF_KS + c, ks + c);
-#pragma unroll
-            for (int c = 0; c < VS; c += 16) {
-                cp_async_16(dst + OFF_VS + c, vs + c);
-                cp_async_16(dst + OFF_VZ + c, vz + c);
-            }
-            cp_async_mbar_arrive(bar);
-            mbar_arrive_expect_tx(bar, TX);
-            tma_load_2d(dst, km, kvh * D, pb * kBS, bar);
-            tma_load_2d(dst + OFF_V, vm, kvh * (D / 2), pb * kBS, bar);
-        } else {
-            // one 3-D box per tile: {128 bytes, 16 rows, D/64 chunks} lands as
-            // D/64 consecutive 2 KB sub-tiles of 128-byte rows, 128B swizzle
-            mbar_arrive_expect_tx(bar, TX);
-            tma_load_3d(dst, km, 0, pb * kBS, kvh * (D / 64), bar);
-            tma_load_3d(dst + OFF_V, vm, 0, pb * kBS, kvh * (D / 64), bar);
-        }
+                                                 const AttnParams&, int kvh, int pb, uint64_t* bar) {
+        // one 3-D box per tile: {128 bytes, 16 rows, D/64 chunks} lands as
+        // D/64 consecutive 2 KB sub-tiles of 128-byte rows, 128B swizzle
+        mbar_arrive_expect_tx(bar, TX);
+        tma_load_3d(dst, km, 0, pb * kBS, kvh * (D / 64), bar);
+        tma_load_3d(dst + OFF_V, vm, 0, pb * kBS, kvh * (D / 64), bar);
     }
 
     __device__ __forceinline__ void init(int) {}
@@ -439,33 +416,17 @@ struct TcMath {
             const int h = valid ? m / QL : 0, j = valid ? m % QL : 0;
             lim[r] = valid ? max(0, ctx - QL + j + 1) : 0;
             const size_t qoff = ((size_t(s) * QL + j) * p.num_heads + kvh * G + h) * D;
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
 #pragma unroll
             for (int kk = 0; kk < NKS; ++kk) {
-                uint32_t lo = 0, hi = 0;
-                if (valid) {
-                    if constexpr (Q8) {
-                        const int d0 = tid * (D / 4) + 4 * kk;   // lane's dims for k-step kk
-                        const float q0 = load_q(p.q, p.q_dtype, qoff + d0), q1 = load_q(p.q, p.q_dtype, qoff + d0 + 1);
-                        const float q2_ = load_q(p.q, p.q_dtype, qoff + d0 + 2),
-                                    q3 = load_q(p.q, p.q_dtype, qoff + d0 + 3);
-                        lo = pack2<false>(q0, q1);
-                        hi = pack2<false>(q2_, q3);
-                    } else {
-                        const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
-                        lo = qw[(qoff + 16 * kk + 2 * tid) / 2];
-                        hi = qw[(qoff + 16 * kk + 8 + 2 * tid) / 2];
-                    }
-                }
-                qa[kk][r] = lo;
-                qa[kk][2 + r] = hi;
+                qa[kk][r] = valid ? qw[(qoff + 16 * kk + 2 * tid) / 2] : 0u;
+                qa[kk][2 + r] = valid ? qw[(qoff + 16 * kk + 8 + 2 * tid) / 2] : 0u;
             }
         }
 #pragma unroll
         for (int n = 0; n < NNT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
         m_run[0] = m_run[1] = -INFINITY;
         l_run[0] = l_run[1] = 0.f;
-#pragma unroll
-        for (int gg = 0; gg < NG; ++gg) zacc[0][gg] = zacc[1][gg] = 0.f;
     }
 
     __device__ __forceinline__ void block(const uint8_t* stg, int pos0, int ntok, uint8_t*, int lane) {
@@ -475,43 +436,17 @@ struct TcMath {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
         // ------------------------------------------------ S = Q K^T
-        if constexpr (Q8) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int t = nt * 8 + g;
-                uint32_t w[NKS];
+        for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-                for (int i = 0; i < D / 64; ++i) {
-                    const int c = tid * (D / 64) + i;
-                    const uint4 v = *reinterpret_cast<const uint4*>(stg + t * D + 16 * swz<D>(c, t));
-                    w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-                }
-#pragma unroll
-                for (int kk = 0; kk < NKS; ++kk) {
-                    uint32_t b0, b1;
-                    s8x4_to_f16x4(w[kk], b0, b1);
-                    mma_f16(sc[nt], qa[kk], b0, b1);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const __half2 ks2 = *reinterpret_cast<const __half2*>(stg + OFF_KS + (nt * 8 + 2 * tid) * 2);
-                const float2 ks = __half22float2(ks2);
-                sc[nt][0] *= ks.x; sc[nt][1] *= ks.y; sc[nt][2] *= ks.x; sc[nt][3] *= ks.y;
-            }
-        } else {
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-#pragma unroll
-                for (int kp = 0; kp < NKS / 2; ++kp) {
-                    const int mi = lane >> 3, r = lane & 7;
-                    const int t = nt * 8 + r, c = 4 * kp + mi;           // 8-dim chunk c
-                    const uint32_t addr = stg_a + (c >> 3) * 2048 + t * 128 + 16 * swz<128>(c & 7, t);
-                    uint32_t R[4];
-                    ldsm_x4(addr, R);
-                    mma16816<BF>(sc[nt], qa[2 * kp], R[0], R[1]);
-                    mma16816<BF>(sc[nt], qa[2 * kp + 1], R[2], R[3]);
-                }
+            for (int kp = 0; kp < NKS / 2; ++kp) {
+                const int mi = lane >> 3, r = lane & 7;
+                const int t = nt * 8 + r, c = 4 * kp + mi;           // 8-dim chunk c
+                const uint32_t addr = stg_a + (c >> 3) * 2048 + t * 128 + 16 * swz<128>(c & 7, t);
+                uint32_t R[4];
+                ldsm_x4(addr, R);
+                mma16816<BF>(sc[nt], qa[2 * kp], R[0], R[1]);
+                mma16816<BF>(sc[nt], qa[2 * kp + 1], R[2], R[3]);
             }
         }
         // ------------------------------------------------ scale, mask, online softmax (rows g, g+8)
@@ -551,115 +486,55 @@ struct TcMath {
                 o[n][0] *= alpha[0]; o[n][1] *= alpha[0];
                 o[n][2] *= alpha[1]; o[n][3] *= alpha[1];
             }
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg) {
-                zacc[0][gg] *= alpha[0];
-                zacc[1][gg] *= alpha[1];
-            }
         }
         // ------------------------------------------------ O += P V
-        if constexpr (Q8) {
-            const int tk[4] = {2 * tid, 2 * tid + 1, 8 + 2 * tid, 9 + 2 * tid};
-            float sv[4][NG], zv[4][NG];
+        // P as the A operand: bf16 keeps 8 significant bits, so P = hi + lo
+        // (two MMAs, P exact to ~2^-17); fp16's 11 bits are kept as one operand.
+        uint32_t a[4], alo[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const bool valid = tk[i] < ntok;   // past the context: NaN metadata, kept out of the MMA
-                const __half* vs = reinterpret_cast<const __half*>(stg + OFF_VS) + tk[i] * NG;
-                const __half* vz = reinterpret_cast<const __half*>(stg + OFF_VZ) + tk[i] * NG;
-#pragma unroll
-                for (int gg = 0; gg < NG; ++gg) {
-                    sv[i][gg] = valid ? __half2float(vs[gg]) : 0.f;
-                    zv[i][gg] = valid ? __half2float(vz[gg]) : 0.f;
-                }
+        for (int i = 0; i < 4; ++i) {
+            const float x = sc[i >> 1][2 * (i & 1)], y = sc[i >> 1][2 * (i & 1) + 1];
+            a[i] = pack2<BF>(x, y);
+            if constexpr (BF) {
+                const float hx = __uint_as_float(a[i] << 16), hy = __uint_as_float(a[i] & 0xffff0000u);
+                alo[i] = pack2<BF>(x - hx, y - hy);
             }
-            uint32_t X[NG], Y[NG];
+        }
+        // V rows past the context may hold anything (NaN): zero them in the operand
+        const uint32_t m01 = (2 * tid < ntok ? 0x0000ffffu : 0u) | (2 * tid + 1 < ntok ? 0xffff0000u : 0u);
+        const uint32_t m23 = (8 + 2 * tid < ntok ? 0x0000ffffu : 0u) | (9 + 2 * tid < ntok ? 0xffff0000u : 0u);
 #pragma unroll
-            for (int g0 = 0; g0 < NG; g0 += 2) {
-                const int mi = lane >> 3, r = lane & 7;
-                const int t = (mi & 1) * 8 + r, c = g0 + (mi >> 1);
-                const uint32_t addr = stg_a + OFF_V + t * (D / 2) + 16 * swz<D / 2>(c, t);
-                uint32_t R[4];
-                ldsm_x4_t(addr, R);
-                X[g0] = R[0]; Y[g0] = R[1]; X[g0 + 1] = R[2]; Y[g0 + 1] = R[3];
+        for (int np = 0; np < NNT / 2; ++np) {
+            const int mi = lane >> 3, r = lane & 7;
+            const int t = (mi & 1) * 8 + r, c = 2 * np + (mi >> 1);   // 8-dim chunk = n-tile
+            const uint32_t addr = stg_a + OFF_V + (c >> 3) * 2048 + t * 128 + 16 * swz<128>(c & 7, t);
+            uint32_t R[4];
+            ldsm_x4_t(addr, R);
+            if (ntok < kBS) {
+                R[0] &= m01; R[1] &= m23; R[2] &= m01; R[3] &= m23;
             }
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg) {
-                uint32_t a[4];
-                a[0] = pack2<false>(sc[0][0] * sv[0][gg], sc[0][1] * sv[1][gg]);
-                a[1] = pack2<false>(sc[0][2] * sv[0][gg], sc[0][3] * sv[1][gg]);
-                a[2] = pack2<false>(sc[1][0] * sv[2][gg], sc[1][1] * sv[3][gg]);
-                a[3] = pack2<false>(sc[1][2] * sv[2][gg], sc[1][3] * sv[3][gg]);
-                zacc[0][gg] += sc[0][0] * zv[0][gg] + sc[0][1] * zv[1][gg] + sc[1][0] * zv[2][gg] + sc[1][1] * zv[3][gg];
-                zacc[1][gg] += sc[0][2] * zv[0][gg] + sc[0][3] * zv[1][gg] + sc[1][2] * zv[2][gg] + sc[1][3] * zv[3][gg];
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    mma_f16(o[4 * gg + i], a, u4pair_to_f16x2(X[gg], i), u4pair_to_f16x2(Y[gg], i));
-            }
-        } else {
-            // P as the A operand: bf16 keeps 8 significant bits, so P = hi + lo
-            // (two MMAs, P exact to ~2^-17); fp16's 11 bits are kept as one operand.
-            uint32_t a[4], alo[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float x = sc[i >> 1][2 * (i & 1)], y = sc[i >> 1][2 * (i & 1) + 1];
-                a[i] = pack2<BF>(x, y);
-                if constexpr (BF) {
-                    const float hx = __uint_as_float(a[i] << 16), hy = __uint_as_float(a[i] & 0xffff0000u);
-                    alo[i] = pack2<BF>(x - hx, y - hy);
-                }
-            }
-            // V rows past the context may hold anything (NaN): zero them in the operand
-            const uint32_t m01 = (2 * tid < ntok ? 0x0000ffffu : 0u) | (2 * tid + 1 < ntok ? 0xffff0000u : 0u);
-            const uint32_t m23 = (8 + 2 * tid < ntok ? 0x0000ffffu : 0u) | (9 + 2 * tid < ntok ? 0xffff0000u : 0u);
-#pragma unroll
-            for (int np = 0; np < NNT / 2; ++np) {
-                const int mi = lane >> 3, r = lane & 7;
-                const int t = (mi & 1) * 8 + r, c = 2 * np + (mi >> 1);   // 8-dim chunk = n-tile
-                const uint32_t addr = stg_a + OFF_V + (c >> 3) * 2048 + t * 128 + 16 * swz<128>(c & 7, t);
-                uint32_t R[4];
-                ldsm_x4_t(addr, R);
-                if (ntok < kBS) {
-                    R[0] &= m01; R[1] &= m23; R[2] &= m01; R[3] &= m23;
-                }
-                mma16816<BF>(o[2 * np], a, R[0], R[1]);
-                mma16816<BF>(o[2 * np + 1], a, R[2], R[3]);
-                if constexpr (BF) {
-                    mma16816<BF>(o[2 * np], alo, R[0], R[1]);
-                    mma16816<BF>(o[2 * np + 1], alo, R[2], R[3]);
-                }
+            mma16816<BF>(o[2 * np], a, R[0], R[1]);
+            mma16816<BF>(o[2 * np + 1], a, R[2], R[3]);
+            if constexpr (BF) {
+                mma16816<BF>(o[2 * np], alo, R[0], R[1]);
+                mma16816<BF>(o[2 * np + 1], alo, R[2], R[3]);
             }
         }
     }
 
-    // K8/V4: add the V zero-point term sum_t p_t z_t (the same for every dim of a group)
-    __device__ __forceinline__ void finish(int lane) {
-        (void)lane;
-        if constexpr (Q8) {
-#pragma unroll
-            for (int gg = 0; gg < NG; ++gg)
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    float z = zacc[r][gg];
-                    z += __shfl_xor_sync(0xffffffffu, z, 1);
-                    z += __shfl_xor_sync(0xffffffffu, z, 2);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        o[4 * gg + i][2 * r] += z;
-                        o[4 * gg + i][2 * r + 1] += z;
-                    }
-                }
-        }
-    }
+    __device__ __forceinline__ void finish(int) {}
 
+    // unnormalised rows [M][D] (ob_idx order) and per-row (m, l) of this warp
     __device__ __forceinline__ void store(float* ob, float* mw, float* lw, int M, int lane) const {
         const int g = lane >> 2, tid = lane & 3;
 #pragma unroll
         for (int n = 0; n < NNT; ++n)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = g + 8 * (e >> 1), col = 2 * tid + (e & 1);
-                const int d = Q8 ? 32 * (n >> 2) + 4 * col + (n & 3) : 8 * n + col;
-                if (m < M) ob[m * D + d] = o[n][e];
+            for (int r = 0; r < 2; ++r) {
+                const int m = g + 8 * r;
+                if (m < M)
+                    *reinterpret_cast<float2*>(ob + ob_idx(m, 8 * n + 2 * tid, D)) =
+                        make_float2(o[n][2 * r], o[n][2 * r + 1]);
             }
         if (tid == 0) {
             if (g < M) {
@@ -970,7 +845,7 @@ struct TqMath {
                 if (q >= M) continue;
 #pragma unroll
                 for (int gg = 0; gg < NG; ++gg)
-                    *reinterpret_cast<float4*>(ob + q * D + 32 * gg + 4 * g) =
+                    *reinterpret_cast<float4*>(ob + ob_idx(q, 32 * gg + 4 * g, D)) =
                         make_float4(o[nt][2 * gg][e], o[nt][2 * gg + 1][e], o[nt][2 * gg][2 + e], o[nt][2 * gg + 1][2 + e]);
                 if (g == 0) {
                     mw[q] = m_run[nt][e];
@@ -1196,7 +1071,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     float* lw = mw + NCW * kMaxRows;                                  // [NCW][16]
     float* rm = lw + NCW * kMaxRows;                                  // [16] merged row max
     float* rl = rm + kMaxRows;                                        // [16] merged row sum
-    float* ob = rl + kMaxRows;                                        // [NCW][M][D]
+    float* ob = rl + kMaxRows;                                        // [NCW][M][D], ob_idx order
     uint8_t* scratch = reinterpret_cast<uint8_t*>(ob + size_t(NCW) * M * D);   // [NCW][SCRATCH]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1354,11 +1229,11 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             const int i4 = tid + k * CT;
             float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
             if (i4 < n4) {
-                const int m = (i4 << 2) / D;
+                const int m = (i4 << 2) / D, d = (i4 << 2) - m * D;
 #pragma unroll
                 for (int w2 = 0; w2 < NCW; ++w2) {
                     const float f = mw[w2 * kMaxRows + m];
-                    const float4 v = reinterpret_cast<const float4*>(ob + size_t(w2) * M * D)[i4];
+                    const float4 v = *reinterpret_cast<const float4*>(ob + size_t(w2) * M * D + ob_idx(m, d, D));
                     O.x = fmaf(v.x, f, O.x);
                     O.y = fmaf(v.y, f, O.y);
                     O.z = fmaf(v.z, f, O.z);
