@@ -102,7 +102,7 @@ def _declare(L):
     L.pkvo_quantize_kv.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I]
     L.pkvo_paged_attention.restype = _I
     L.pkvo_paged_attention.argtypes = ([_P, _P, _P, _P, _I, _I, _P, _I, _I, _D, _I] + [_P] * 5 +
-                                       [_I] * 5 + [_P, _P, _I, _I, _I, _P, _I, _I])
+                                       [_I] * 5 + [_P, _P, _I, _I, _I, _P, _I, _I, _I])
     L.pkvo_lse_reduce.restype = None
     L.pkvo_lse_reduce.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I]
 
@@ -222,14 +222,16 @@ def paged_attention(q_bits: np.ndarray, q_dtype: int, scale: float, cache_kind: 
                     k_cache, v_cache, block_tables, context_lens, q_len: int = 1,
                     k_scale=None, v_scale=None, v_zero=None, v_group: int = 32,
                     partition_size: int = 0, max_partitions: int = 0, rows=None,
-                    threads: int = 1, want_out: bool = True):
+                    threads: int = 1, want_out: bool = True, window: int = 0):
     """fp64 paged attention.
 
     q_bits: [R, H, D] raw bits (uint16) for F16/BF16 (or float32/float64 with
     q_dtype F32/F64).  k_cache / v_cache: [NB, bs, Hkv, D] uint16 bits (f16/bf16
     caches) or the K8/V4 code arrays.  Returns ``out`` [R, H, D] (NaN in rows
     not computed when ``rows`` is given) and, if partition_size > 0,
-    (part_o, part_m, part_l).
+    (part_o, part_m, part_l).  window > 0 keeps the last ``window`` stored
+    tokens of each sequence visible (partitions wholly before them come back
+    empty: o = 0, m = -inf, l = 0).
     """
     q = np.ascontiguousarray(q_bits)
     R, H, D = q.shape
@@ -253,7 +255,7 @@ def paged_attention(q_bits: np.ndarray, q_dtype: int, scale: float, cache_kind: 
         float(scale), cache_kind, _ptr(np.ascontiguousarray(k_cache)),
         _ptr(np.ascontiguousarray(v_cache)), _ptr(k_scale), _ptr(v_scale), _ptr(v_zero), NB, bs,
         Hkv, D, v_group, _ptr(bt), _ptr(cl), bt.shape[0], bt.shape[1], q_len, _ptr(rl),
-        0 if rl is None else rl.size, threads)
+        0 if rl is None else rl.size, threads, int(window))
     if rc:
         raise ValueError(f"oracle attention failed ({rc})")
     if part is not None:

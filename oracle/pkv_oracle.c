@@ -301,6 +301,7 @@ typedef struct {
     /* sequences */
     const int32_t *block_tables, *context_lens;
     int num_seqs, max_blocks, q_len;
+    int window;   /* sliding window in tokens, 0 = none */
     /* work */
     const int32_t *row_list;
     int n_rows, n_threads, thread_id;
@@ -409,11 +410,19 @@ static void *attn_worker(void *arg)
          * Offset Tracking": kernels read only the tokens stored so far]. */
         int vis = ctx - J->q_len + j + 1;
         if (vis < 0) vis = 0;
+        /* Sliding window: the visible part of the cache is trimmed to its last
+         * `window` stored tokens; older ones are masked, not freed [MTPLX-2
+         * §"Sliding-Window Memory Control" and the FAQ on adjusting the window].
+         * The trim is of the stored cache (the last `window` of its ctx tokens),
+         * so every draft row of a verify block starts at the same token. */
+        int lo = 0;
+        if (J->window > 0 && ctx > J->window) lo = ctx - J->window;
+        if (lo > vis) lo = vis;
         int kvh = h / g;
         size_t qoff = ((size_t)r * H + h) * D;
         for (int d = 0; d < D; d++) qd[d] = load_elem(J->q, J->q_dtype, qoff + d);
         if (J->out) {
-            if (attend_range(J, s, kvh, qd, 0, vis, J->out + qoff, &m, &l, x, row)) { J->error = -1; break; }
+            if (attend_range(J, s, kvh, qd, lo, vis, J->out + qoff, &m, &l, x, row)) { J->error = -1; break; }
         }
         if (J->part_o) {
             /* Split-KV: partition p covers logical tokens [pP, (p+1)P) of the
@@ -421,7 +430,7 @@ static void *attn_worker(void *arg)
              * splits; METAL: "split-KV decode kernels"]. */
             int P = J->partition_size;
             for (int p = 0; p < J->max_partitions; p++) {
-                int t0 = p * P, t1 = (p + 1) * P < vis ? (p + 1) * P : vis;
+                int t0 = p * P > lo ? p * P : lo, t1 = (p + 1) * P < vis ? (p + 1) * P : vis;
                 size_t pi = ((size_t)r * H + h) * J->max_partitions + p;
                 if (attend_range(J, s, kvh, qd, t0, t1, J->part_o + pi * D, &J->part_m[pi],
                                  &J->part_l[pi], x, row)) { J->error = -1; break; }
@@ -441,7 +450,8 @@ static void *attn_worker(void *arg)
  * are written to part_o [R, H, max_partitions, D] and part_m / part_l
  * [R, H, max_partitions] (m_p in the units of scale * q.k, natural log base).
  * row_list (optional) restricts the work to the listed rows; the other rows of
- * out are left untouched.  Returns 0, or a negative code on an out-of-range
+ * out are left untouched.  window > 0 keeps only the last `window` stored tokens
+ * of each sequence visible.  Returns 0, or a negative code on an out-of-range
  * block id (-1) or a context longer than its table (-2). */
 int pkvo_paged_attention(double *out, double *part_o, double *part_m, double *part_l,
                          int partition_size, int max_partitions, const void *q, int q_dtype,
@@ -450,15 +460,16 @@ int pkvo_paged_attention(double *out, double *part_o, double *part_m, double *pa
                          const void *v_zero, int num_blocks, int block_size, int num_kv_heads,
                          int head_dim, int v_group, const int32_t *block_tables,
                          const int32_t *context_lens, int num_seqs, int max_blocks, int q_len,
-                         const int32_t *row_list, int n_rows, int n_threads)
+                         const int32_t *row_list, int n_rows, int n_threads, int window)
 {
+    if (window < 0) return -3;
     if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -3;
     if (part_o && partition_size <= 0) return -3;
     if (n_threads < 1) n_threads = 1;
     attn_job base = {out, part_o, part_m, part_l, partition_size, max_partitions, q, q_dtype,
                      num_heads, scale, cache_kind, k_cache, v_cache, k_scale, v_scale, v_zero,
                      num_blocks, block_size, num_kv_heads, head_dim, v_group, block_tables,
-                     context_lens, num_seqs, max_blocks, q_len, row_list, n_rows, n_threads, 0, 0};
+                     context_lens, num_seqs, max_blocks, q_len, window, row_list, n_rows, n_threads, 0, 0};
     attn_job *jobs = (attn_job *)malloc(sizeof(attn_job) * (size_t)n_threads);
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
     for (int i = 0; i < n_threads; i++) {

@@ -56,6 +56,7 @@ class Workload:
     v_new: Optional[torch.Tensor] = None
     slot_new: Optional[torch.Tensor] = None  # int64 [T]
     partition_size: int = 0                  # 0: single pass
+    sliding_window: int = 0                  # 0: every stored token is visible
     block_size: int = BLOCK_SIZE
     v_group: int = 32
     notes: List[str] = field(default_factory=list)
@@ -103,7 +104,7 @@ def build(*, name: str, seed: int, context_lens: List[int], num_heads: int, num_
           num_blocks: Optional[int] = None, max_blocks: Optional[int] = None,
           new_tokens: str = "tail", value_scale: float = 1.0, spike_frac: float = 0.0,
           spike_scale: float = 8.0, partition_size: int = 0, identity_table: bool = False,
-          device: str = "cpu", scale: Optional[float] = None) -> Workload:
+          device: str = "cpu", scale: Optional[float] = None, sliding_window: int = 0) -> Workload:
     """General seeded workload.
 
     new_tokens:
@@ -169,7 +170,7 @@ def build(*, name: str, seed: int, context_lens: List[int], num_heads: int, num_
     w = Workload(name=name, cache=cache, src_dtype=src_dtype, num_seqs=B, num_heads=H,
                  num_kv_heads=Hkv, head_dim=D, num_blocks=num_blocks, q_len=q_len,
                  scale=(1.0 / math.sqrt(D)) if scale is None else scale, block_tables=table,
-                 context_lens=ctx, q=q, partition_size=partition_size)
+                 context_lens=ctx, q=q, partition_size=partition_size, sliding_window=sliding_window)
     T = int(slot_new.numel())
     if cache in ("f16", "bf16"):
         # 6./7. K and V pools, then NaN everywhere but the history slots

@@ -43,6 +43,8 @@ def sdpa_reference(w, cs):
         Q = q64[s * w.q_len:(s + 1) * w.q_len].transpose(0, 1)          # [H, q_len, D]
         j = torch.arange(w.q_len)[:, None]
         mask = t[None, :] < (c - w.q_len + j + 1)                        # [q_len, c]
+        if w.sliding_window > 0:                                         # last W stored tokens
+            mask = mask & (t[None, :] >= c - w.sliding_window)
         o = F.scaled_dot_product_attention(Q, K, V, attn_mask=mask, scale=w.scale)
         empty = ~mask.any(1)
         o[:, empty] = 0.0
@@ -218,3 +220,88 @@ def test_nan_sentinel_reaches_output_when_read():
     cs = oracle_cache_after_step(w)
     w.context_lens = torch.tensor([21], dtype=torch.int32)
     assert np.isnan(oracle_attention(w, cs)).all()
+
+
+# ---------------------------------------------------------------- sliding window
+# [MTPLX-2 §"Sliding-Window Memory Control": the visible part of the cache is
+#  trimmed to the last `window` stored tokens; older ones are masked.]
+
+WINDOW_CASES = [
+    # (ctx list, H, Hkv, D, q_len, dtype, window)
+    ([1, 15, 16, 17, 40, 100], 4, 2, 64, 1, "f16", 16),
+    ([33, 7, 64, 200], 8, 2, 128, 1, "bf16", 17),
+    ([9, 40, 4, 70], 8, 2, 64, 3, "bf16", 20),
+    ([64, 17, 130], 8, 8, 128, 2, "f16", 5),
+    ([50, 3], 4, 4, 64, 1, "bf16", 1),
+]
+
+
+@pytest.mark.parametrize("ctx,H,Hkv,D,ql,dt,win", WINDOW_CASES)
+def test_window_matches_sdpa_over_the_last_tokens(ctx, H, Hkv, D, ql, dt, win):
+    w = W.build(name="t", seed=21, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
+                cache=dt, q_len=ql, sliding_window=win)
+    cs = oracle_cache_after_step(w)
+    got = oracle_attention(w, cs)
+    ref = sdpa_reference(w, cs)
+    assert np.isfinite(got).all()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
+def test_window_at_least_the_context_changes_nothing():
+    kw = dict(name="t", seed=22, context_lens=[1, 31, 64, 97], num_heads=8, num_kv_heads=2,
+              head_dim=64, cache="bf16", q_len=2)
+    w0 = W.build(**kw)
+    cs = oracle_cache_after_step(w0)
+    base = oracle_attention(w0, cs)
+    for win in (97, 98, 4096):
+        w = W.build(**kw, sliding_window=win)
+        assert np.array_equal(oracle_attention(w, cs), base)
+
+
+def test_window_of_one_token_returns_its_v():
+    w = W.build(name="t", seed=23, context_lens=[5, 40, 1], num_heads=4, num_kv_heads=2, head_dim=64,
+                cache="bf16", sliding_window=1)
+    cs = oracle_cache_after_step(w)
+    got = oracle_attention(w, cs)
+    v = oracle.bf16_bits_to_f64(cs["v"]).reshape(-1, 2, 64)
+    table = np_i32(w.block_tables)
+    for s in range(w.num_seqs):
+        t = int(w.context_lens[s]) - 1
+        slot = int(table[s, t // 16]) * 16 + t % 16
+        for h in range(4):
+            assert np.array_equal(got[s, h], v[slot, h // 2])
+
+
+def test_window_equals_shorter_table_of_the_last_tokens():
+    # dropping the first ctx-W tokens (whole blocks) from the table leaves the
+    # same visible set when ctx-W is a multiple of 16
+    w = W.build(name="t", seed=24, context_lens=[80, 48], num_heads=4, num_kv_heads=2, head_dim=64,
+                cache="f16", sliding_window=32)
+    cs = oracle_cache_after_step(w)
+    got = oracle_attention(w, cs)
+    table = np_i32(w.block_tables)
+    short = np.full_like(table, -1)
+    short[0, :2] = table[0, 3:5]
+    short[1, :2] = table[1, 1:3]
+    conv = oracle.f16_bits_to_f64
+    ref = oracle.paged_attention(bits(w.q), oracle.F16, w.scale, oracle.CACHE_F16, cs["k"], cs["v"],
+                                 short, np.array([32, 32], np.int32))
+    np.testing.assert_array_equal(got, ref)
+
+
+@pytest.mark.parametrize("P", [16, 48, 64])
+def test_window_split_partials_reduce_to_single_pass(P):
+    w = W.build(name="t", seed=25, context_lens=[1, 95, 160, 17, 200], num_heads=4, num_kv_heads=2,
+                head_dim=64, cache="bf16", q_len=2, sliding_window=37)
+    cs = oracle_cache_after_step(w)
+    single = oracle_attention(w, cs)
+    NP = -(-w.max_blocks * 16 // P)
+    _, (po, pm, pl) = oracle_attention(w, cs, partition_size=P, max_partitions=NP)
+    np.testing.assert_allclose(oracle.lse_reduce(po, pm, pl), single, rtol=1e-12, atol=1e-14)
+    # partitions wholly before the window are empty
+    for s in range(w.num_seqs):
+        lo = max(0, int(w.context_lens[s]) - 37)
+        for p in range(NP):
+            if (p + 1) * P <= lo:
+                rows = slice(s * 2, s * 2 + 2)
+                assert np.isneginf(pm[rows, :, p]).all() and not pl[rows, :, p].any()

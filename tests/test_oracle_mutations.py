@@ -31,6 +31,12 @@ MUTANTS = [
      lambda: TA.test_split_partials_and_reduce_equal_single_pass(32)),
     ("softmax max not subtracted in weights", "double w = exp(x[t - t0] - m);", "double w = exp(x[t - t0]);",
      lambda: TA.test_split_partials_and_reduce_equal_single_pass(16)),
+    ("window one token short", "if (J->window > 0 && ctx > J->window) lo = ctx - J->window;",
+     "if (J->window > 0 && ctx > J->window) lo = ctx - J->window + 1;",
+     lambda: TA.test_window_matches_sdpa_over_the_last_tokens(*TA.WINDOW_CASES[0])),
+    ("window per draft row", "if (J->window > 0 && ctx > J->window) lo = ctx - J->window;",
+     "if (J->window > 0 && vis > J->window) lo = vis - J->window;",
+     lambda: TA.test_window_matches_sdpa_over_the_last_tokens(*TA.WINDOW_CASES[2])),
 ]
 
 
