@@ -39,13 +39,15 @@ WORKLOADS = {
     "long_context_32k": 3,
     "k8v4_batch32": 4,
     "verify_batch256": 5,
+    "sliding_window_b8_w4096": "sliding_window_b8_w4096",
 }
 DEFAULT_WORKLOAD = "llama3_8b_batch8"
 # schedule of the attention call per workload: the 32K workload is defined with
 # fixed 512-token partitions and a separate reduce; the batched ones use the
 # balanced split with its fused combine; the tiny one is a single pass
 DEFAULT_SCHEDULE = {"tiny_f16": "single", "llama3_8b_batch8": "balanced", "long_context_32k": "split",
-                    "k8v4_batch32": "balanced", "verify_batch256": "balanced"}
+                    "k8v4_batch32": "balanced", "verify_batch256": "balanced",
+                    "sliding_window_b8_w4096": "balanced"}
 KERNEL_NAME = {"single": "pkv_paged_attention", "split": "pkv_paged_attention_split",
                "balanced": "pkv_paged_attention_balanced"}
 
@@ -90,7 +92,8 @@ def dist_env():
 
 def make_workload(name, device, seed_offset=0, partition=None):
     from paged_decode_attention_cache_gb300 import workloads as W
-    fn = W.CONFIGS[WORKLOADS[name]]
+    key = WORKLOADS[name]
+    fn = W.CONFIGS[key] if isinstance(key, int) else W.EXTRA[key]
     kw = {}
     if partition is not None and name != "tiny_f16":
         kw["partition_size"] = partition
@@ -106,7 +109,8 @@ def make_workload(name, device, seed_offset=0, partition=None):
 def step_bytes(w):
     from paged_decode_attention_cache_gb300 import bytes_model as BM
     ctx = [int(c) for c in w.context_lens.cpu()]
-    attn = BM.attention_bytes(ctx, w.q_len, w.num_heads, w.num_kv_heads, w.head_dim, w.cache)
+    attn = BM.attention_bytes(ctx, w.q_len, w.num_heads, w.num_kv_heads, w.head_dim, w.cache,
+                              sliding_window=w.sliding_window)
     wr = BM.write_bytes(int(w.slot_new.numel()), w.num_kv_heads, w.head_dim, w.cache)
     return attn, wr
 

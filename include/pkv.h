@@ -115,6 +115,12 @@ typedef struct pkv_cache {
  *                 speculative verify block [MLXCEL §"Matrix-Absorbed MLA Decode",
  *                 §"Speculative Rewind"], where draft j of sequence s sees the
  *                 tokens [0, context_lens[s] - q_len + j + 1) (causal).
+ *   sliding_window  0: every stored token is visible.  W > 0: only the last W
+ *                 stored tokens, [max(0, context_lens[s] - W), context_lens[s]),
+ *                 are visible (older ones are masked, their blocks not read)
+ *                 [MTPLX-2 §"Sliding-Window Memory Control"]; the trim is of the
+ *                 stored cache, so every draft row starts at the same token.
+ *                 Negative: PKV_ERR_INVALID_ARG.  pkv_gather_kv_cache ignores it.
  */
 typedef struct pkv_seqs {
     const int32_t *block_tables;
@@ -122,6 +128,7 @@ typedef struct pkv_seqs {
     int32_t num_seqs;
     int32_t max_blocks_per_seq;
     int32_t q_len;
+    int32_t sliding_window;
 } pkv_seqs;
 
 /*

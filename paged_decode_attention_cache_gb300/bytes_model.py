@@ -30,16 +30,26 @@ def row_bytes(cache: str, head_dim: int, v_group: int = 32):
 
 
 def attention_bytes(context_lens, q_len: int, num_heads: int, num_kv_heads: int, head_dim: int,
-                    cache: str, q_bytes: int = 2, out_bytes: int = 2, v_group: int = 32) -> int:
+                    cache: str, q_bytes: int = 2, out_bytes: int = 2, v_group: int = 32,
+                    sliding_window: int = 0) -> int:
     """K + V rows of every visible token, q in, out back, block table and lengths.
 
     K and V are counted once per (token, kv head): one CTA serves all query
-    heads of a kv head, so a group's heads share the read."""
+    heads of a kv head, so a group's heads share the read.  With a sliding
+    window only the last ``sliding_window`` stored tokens (and their blocks'
+    table entries) count."""
     kb, vb = row_bytes(cache, head_dim, v_group)
-    kv = sum(int(c) for c in context_lens) * num_kv_heads * (kb + vb)
+
+    def span(c):
+        c = int(c)
+        lo = c - sliding_window if (sliding_window > 0 and c > sliding_window) else 0
+        return lo, c
+
+    kv = sum(c - lo for lo, c in map(span, context_lens)) * num_kv_heads * (kb + vb)
     rows = len(context_lens) * q_len
     qo = rows * num_heads * head_dim * (q_bytes + out_bytes)
-    tables = 4 * sum(-(-int(c) // BLOCK_SIZE) for c in context_lens) + 4 * len(context_lens)
+    tables = 4 * sum(-(-c // BLOCK_SIZE) - lo // BLOCK_SIZE for lo, c in map(span, context_lens)) \
+        + 4 * len(context_lens)
     return kv + qo + tables
 
 

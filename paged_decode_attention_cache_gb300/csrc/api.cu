@@ -84,6 +84,7 @@ pkv_status check_seqs(const pkv_seqs* s) {
     if (!s) return fail(PKV_ERR_INVALID_ARG, "seqs is NULL");
     if (s->num_seqs < 0 || s->num_seqs > 65535) return fail(PKV_ERR_INVALID_ARG, "num_seqs %d", s->num_seqs);
     if (s->q_len < 1) return fail(PKV_ERR_INVALID_ARG, "q_len %d", s->q_len);
+    if (s->sliding_window < 0) return fail(PKV_ERR_INVALID_ARG, "sliding_window %d", s->sliding_window);
     if (s->max_blocks_per_seq < 1) return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d", s->max_blocks_per_seq);
     if (int64_t(s->max_blocks_per_seq) * 16 > INT32_MAX / 2)
         return fail(PKV_ERR_INVALID_ARG, "max_blocks_per_seq %d too large", s->max_blocks_per_seq);
@@ -211,6 +212,7 @@ pkv_status attn_setup(pkv::AttnParams* p, const void* q, pkv_dtype q_dtype, int3
     p->context_lens = seqs->context_lens;
     p->num_seqs = seqs->num_seqs;
     p->max_blocks = seqs->max_blocks_per_seq;
+    p->window = seqs->sliding_window;
     p->err = err;
     return PKV_OK;
 }
@@ -505,6 +507,7 @@ pkv_status pkv_reduce(void* out, pkv_dtype out_dtype, const float* tmp_out, cons
     p.head_dim = head_dim;
     p.partition_size = partition_size;
     p.max_partitions = max_partitions;
+    p.window = seqs->sliding_window;
     return cuda_result(pkv::launch_reduce(p, reinterpret_cast<cudaStream_t>(stream)), "reduce launch");
 }
 

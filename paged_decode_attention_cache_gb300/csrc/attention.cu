@@ -196,6 +196,7 @@ struct CcMath {
 
     float2 q2[G][CPL * 4];
     float m_run, l_run;            // for head lane % G
+    int lo_;                       // first visible token (sliding window)
     float2 acc[G][DPL / 2];
     int my_head;
     bool writer;
@@ -217,8 +218,9 @@ struct CcMath {
         writer = (jl & (LPT / G - 1)) == 0;
     }
 
-    __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int /*ctx*/, int lane) {
+    __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
         const int jl = lane % LPT;
+        lo_ = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
         const T* qrow = reinterpret_cast<const T*>(p.q) + (size_t(s) * p.num_heads + kvh * G) * D;
 #pragma unroll
         for (int h = 0; h < G; ++h)
@@ -240,7 +242,7 @@ struct CcMath {
             for (int e = 0; e < DPL / 2; ++e) acc[h][e] = make_float2(0.f, 0.f);
     }
 
-    __device__ __forceinline__ void block(const uint8_t* stg, int /*pos0*/, int ntok, uint8_t* scratch, int lane) {
+    __device__ __forceinline__ void block(const uint8_t* stg, int pos0, int ntok, uint8_t* scratch, int lane) {
         float* sc = reinterpret_cast<float*>(scratch);
         float2* pc = reinterpret_cast<float2*>(scratch + kBS * G * 4);
         float* alph = reinterpret_cast<float*>(scratch + kBS * G * 12);
@@ -284,7 +286,7 @@ struct CcMath {
                     a[0] += __shfl_xor_sync(0xffffffffu, a[0], o);
                 }
             }
-            if (writer) sc[t * G + my_head] = (t < ntok) ? a[0] : -INFINITY;
+            if (writer) sc[t * G + my_head] = (t < ntok && pos0 + t >= lo_) ? a[0] : -INFINITY;
         }
         __syncwarp();
         // ---- online softmax over the block's 16 x G scores
@@ -393,6 +395,7 @@ struct TcMath {
     float o[NNT][4];
     float m_run[2], l_run[2];
     int lim[2];
+    int lo_;   // first visible token (sliding window)
 
     static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
                                                  const AttnParams&, int kvh, int pb, uint64_t* bar) {
@@ -417,6 +420,7 @@ struct TcMath {
             lim[r] = valid ? max(0, ctx - QL + j + 1) : 0;
             const size_t qoff = ((size_t(s) * QL + j) * p.num_heads + kvh * G + h) * D;
             const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+            lo_ = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
 #pragma unroll
             for (int kk = 0; kk < NKS; ++kk) {
                 qa[kk][r] = valid ? qw[(qoff + 16 * kk + 2 * tid) / 2] : 0u;
@@ -455,7 +459,7 @@ struct TcMath {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int pos = pos0 + nt * 8 + 2 * tid + (e & 1);
-                sc[nt][e] = (pos < lim[e >> 1]) ? sc[nt][e] * scale_log2_ : -INFINITY;
+                sc[nt][e] = (pos < lim[e >> 1] && pos >= lo_) ? sc[nt][e] * scale_log2_ : -INFINITY;
             }
         float alpha[2];
 #pragma unroll
@@ -610,6 +614,7 @@ struct TqMath {
     float cz[NT][4];           // Z^T P^T: rows = groups
     float m_run[NT][2], l_part[NT][2];   // per query column 2t, 2t+1 (l: this thread's tokens)
     int lim[NT][2];
+    int lo_;   // first visible token (sliding window)
     float scale_log2_;
 
     static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
@@ -637,6 +642,7 @@ struct TqMath {
     __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
         const int g = lane >> 2, t = lane & 3;
         const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL;
+        lo_ = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int n = 8 * nt + g;
@@ -699,10 +705,10 @@ struct TqMath {
         const int pg = pos0 + g, pg8 = pos0 + g + 8;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            sc[nt][0] = (pg < lim[nt][0]) ? sc[nt][0] * k0 : -INFINITY;
-            sc[nt][1] = (pg < lim[nt][1]) ? sc[nt][1] * k0 : -INFINITY;
-            sc[nt][2] = (pg8 < lim[nt][0]) ? sc[nt][2] * k1 : -INFINITY;
-            sc[nt][3] = (pg8 < lim[nt][1]) ? sc[nt][3] * k1 : -INFINITY;
+            sc[nt][0] = (pg < lim[nt][0] && pg >= lo_) ? sc[nt][0] * k0 : -INFINITY;
+            sc[nt][1] = (pg < lim[nt][1] && pg >= lo_) ? sc[nt][1] * k0 : -INFINITY;
+            sc[nt][2] = (pg8 < lim[nt][0] && pg8 >= lo_) ? sc[nt][2] * k1 : -INFINITY;
+            sc[nt][3] = (pg8 < lim[nt][1] && pg8 >= lo_) ? sc[nt][3] * k1 : -INFINITY;
         }
         // ------------------------------------------------ online softmax per query column
         float alpha[NT][2];
@@ -863,13 +869,27 @@ __device__ __forceinline__ int seq_ctx(const AttnParams& p, int s) {
     return c < 0 ? 0 : (c > cap ? cap : c);
 }
 
-// units of a sequence of nb blocks: balanced = blocks; split = partitions
-__device__ __forceinline__ long long seq_units(const AttnParams& p, int nb) {
-    return p.mode == kModeBalanced ? nb : (nb + p.partition_blocks - 1) / p.partition_blocks;
+// First visible token of a sequence: a sliding window keeps the last `window`
+// stored tokens [MTPLX-2 §"Sliding-Window Memory Control"].
+__device__ __forceinline__ int seq_lo(const AttnParams& p, int ctx) {
+    return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+}
+
+// First unit of a sequence (blocks / partitions wholly before the window are
+// skipped) and its number of units: balanced = blocks; split = partitions.
+__device__ __forceinline__ int seq_first_unit(const AttnParams& p, int ctx) {
+    const int b = seq_lo(p, ctx) / kBS;
+    return p.mode == kModeBalanced ? b : b / p.partition_blocks;
+}
+__device__ __forceinline__ long long seq_units(const AttnParams& p, int ctx) {
+    const int nb = (ctx + kBS - 1) / kBS;
+    const int all = p.mode == kModeBalanced ? nb : (nb + p.partition_blocks - 1) / p.partition_blocks;
+    return all - seq_first_unit(p, ctx);
 }
 
 struct Seg {
     int s, kvh, b0, b1, nb, ctx, part;
+    long long nu;           // units of this (sequence, kv head) pair
     long long pair_start;   // balanced: the sequence's first unit (block) in the lane's list
     long long cost_base;    // balanced: unit u of this pair sits at cost position u + cost_base
     bool whole;             // the segment is the whole pair
@@ -884,6 +904,7 @@ struct SegIter {
     long long start;     // its first unit
     long long n;         // its units
     int nb, ctx;
+    int u_first;         // first unit (block or partition) of s
     int r;               // non-empty sequences before s in the lane's list
 
     __device__ __forceinline__ void load_seq(const AttnParams& p, int s_, long long start_, int known_ctx = -1) {
@@ -892,9 +913,10 @@ struct SegIter {
         if (s < p.num_seqs) {
             ctx = known_ctx >= 0 ? known_ctx : seq_ctx(p, s);
             nb = (ctx + kBS - 1) / kBS;
-            n = seq_units(p, nb);
+            u_first = seq_first_unit(p, ctx);
+            n = seq_units(p, ctx);
         } else {
-            ctx = nb = 0;
+            ctx = nb = u_first = 0;
             n = 0;
         }
     }
@@ -907,8 +929,9 @@ struct SegIter {
             g.kvh = int(u % Hkv);
             g.ctx = seq_ctx(p, g.s);
             g.nb = (g.ctx + kBS - 1) / kBS;
-            g.b0 = 0;
+            g.b0 = seq_lo(p, g.ctx) / kBS;
             g.b1 = g.nb;
+            g.nu = 1;
             g.part = 0;
             g.pair_start = 0;
             g.cost_base = 0;
@@ -929,19 +952,20 @@ struct SegIter {
         g.kvh = kvh;
         g.nb = nb;
         g.ctx = ctx;
+        g.nu = n;
         if (p.mode == kModeBalanced) {
             const long long k1 = (n < k + (u1 - u)) ? n : k + (u1 - u);
-            g.b0 = int(k);
-            g.b1 = int(k1);
+            g.b0 = u_first + int(k);
+            g.b1 = u_first + int(k1);
             g.part = 0;
             g.pair_start = start;
             g.cost_base = (long long)p.seg_cost * (r + 1);
             g.whole = (k == 0 && k1 == n);
             u += k1 - k;
         } else {
-            g.part = int(k);
-            g.b0 = int(k) * p.partition_blocks;
-            g.b1 = min(nb, g.b0 + p.partition_blocks);
+            g.part = u_first + int(k);
+            g.b0 = max(g.part * p.partition_blocks, seq_lo(p, ctx) / kBS);
+            g.b1 = min(nb, (g.part + 1) * p.partition_blocks);
             g.pair_start = 0;
             g.cost_base = 0;
             g.whole = false;
@@ -976,7 +1000,7 @@ __device__ __forceinline__ SeqPos plan_round(const AttnParams& p, int r0, long l
     SeqPos sp;
     sp.s = r0 + threadIdx.x;
     sp.ctx = sp.s < p.num_seqs ? seq_ctx(p, sp.s) : 0;
-    sp.u = sp.s < p.num_seqs ? seq_units(p, (sp.ctx + kBS - 1) / kBS) : 0;
+    sp.u = sp.s < p.num_seqs ? seq_units(p, sp.ctx) : 0;
     const unsigned long long v =
         sp.u > 0 ? ((unsigned long long)(sp.u + p.seg_cost) << 32) | (unsigned long long)sp.u : 0ull;
     unsigned long long incl = v;
@@ -1291,7 +1315,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             __threadfence();
             named_barrier_sync(1, CT);
             const int c_lo = int((sg.pair_start + sg.cost_base) / chunk),
-                      c_hi = int((sg.pair_start + sg.nb - 1 + sg.cost_base) / chunk);
+                      c_hi = int((sg.pair_start + sg.nu - 1 + sg.cost_base) / chunk);
             const int np = c_hi - c_lo + 1;
             if (tid == 0) {
                 const int prev = atomicAdd(&p.counters[pair], 1);

@@ -60,6 +60,7 @@ struct AttnParams {
     const int32_t* context_lens;
     int32_t num_seqs;
     int32_t max_blocks;
+    int32_t window;     // sliding window in tokens, 0 = none
     uint32_t* err;
     // persistent scheduling
     int32_t mode;       // kModeSingle / kModeSplit / kModeBalanced
@@ -103,6 +104,7 @@ struct ReduceParams {
     int32_t head_dim;
     int32_t partition_size;
     int32_t max_partitions;
+    int32_t window;     // sliding window in tokens, 0 = none
 };
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream);
 

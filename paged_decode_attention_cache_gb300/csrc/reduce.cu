@@ -37,7 +37,10 @@ __global__ void __launch_bounds__(kThreads) lse_reduce_kernel(ReduceParams p) {
     if (ctx < 0) ctx = 0;
     int nparts = (ctx + p.partition_size - 1) / p.partition_size;
     if (nparts > p.max_partitions) nparts = p.max_partitions;
-    const size_t base = (size_t(r) * p.num_heads + h) * p.max_partitions;
+    // sliding window: partitions wholly before the last `window` tokens were not written
+    const int p_first = (p.window > 0 && ctx > p.window) ? (ctx - p.window) / p.partition_size : 0;
+    nparts = nparts > p_first ? nparts - p_first : 0;
+    const size_t base = (size_t(r) * p.num_heads + h) * p.max_partitions + p_first;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     // M = max over partitions with weight

@@ -41,7 +41,8 @@ class _Cache(ctypes.Structure):
 
 class _Seqs(ctypes.Structure):
     _fields_ = [("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
-                ("num_seqs", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("q_len", ctypes.c_int32)]
+                ("num_seqs", ctypes.c_int32), ("max_blocks_per_seq", ctypes.c_int32), ("q_len", ctypes.c_int32),
+                ("sliding_window", ctypes.c_int32)]
 
 
 _lib = None
@@ -161,12 +162,13 @@ class Seqs:
     block_tables: torch.Tensor   # int32 [B, max_blocks]
     context_lens: torch.Tensor   # int32 [B]
     q_len: int = 1
+    sliding_window: int = 0      # 0: none; W: only the last W stored tokens are visible
 
     def c_struct(self) -> _Seqs:
         if self.block_tables.dtype != torch.int32 or self.context_lens.dtype != torch.int32:
             raise ValueError("block_tables and context_lens must be int32")
         return _Seqs(_ptr(self.block_tables), _ptr(self.context_lens), int(self.block_tables.shape[0]),
-                     int(self.block_tables.shape[1]), int(self.q_len))
+                     int(self.block_tables.shape[1]), int(self.q_len), int(self.sliding_window))
 
 
 def _err_ptr(err: Optional[torch.Tensor]):

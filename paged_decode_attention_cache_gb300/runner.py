@@ -37,7 +37,8 @@ class DecodeStep:
         if schedule != "split":
             self.partition_size = 0
         self.schedule = schedule
-        self.seqs = ops.Seqs(w.block_tables.to(dev).contiguous(), w.context_lens.to(dev).contiguous(), w.q_len)
+        self.seqs = ops.Seqs(w.block_tables.to(dev).contiguous(), w.context_lens.to(dev).contiguous(), w.q_len,
+                             w.sliding_window)
         self.q = w.q.to(dev).contiguous()
         self.k_new = w.k_new.to(dev).contiguous()
         self.v_new = w.v_new.to(dev).contiguous()

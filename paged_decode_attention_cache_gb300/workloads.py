@@ -260,5 +260,18 @@ def verify_batch256(device="cpu", seed=5, partition_size=512) -> Workload:
                  max_blocks=1024, partition_size=partition_size, device=device)
 
 
+def sliding_window_b8_w4096(device="cpu", seed=6, partition_size=512) -> Workload:
+    """Sliding-window decode: batch 8, contexts uniform in [8192, 32768], only the last
+    4096 stored tokens visible, 32/8 heads, head_dim 128, bf16, values N(0,1) * 0.5, one
+    new token per sequence."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 7)
+    ctx = _uniform_ints(g, 8, 8192, 32768)
+    return build(name="window4096_b8_h32kv8_d128_bf16", seed=seed, context_lens=ctx, num_heads=32,
+                 num_kv_heads=8, head_dim=128, cache="bf16", max_blocks=2048, value_scale=0.5,
+                 partition_size=partition_size, sliding_window=4096, device=device)
+
+
 CONFIGS = {1: tiny_f16, 2: llama3_8b_batch8, 3: long_context_32k, 4: k8v4_batch32,
            5: verify_batch256}
+# workloads beyond the five configurations (rows ranked next)
+EXTRA = {"sliding_window_b8_w4096": sliding_window_b8_w4096}
