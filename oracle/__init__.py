@@ -103,6 +103,8 @@ def _declare(L):
     L.pkvo_paged_attention.restype = _I
     L.pkvo_paged_attention.argtypes = ([_P, _P, _P, _P, _I, _I, _P, _I, _I, _D, _I] + [_P] * 5 +
                                        [_I] * 5 + [_P, _P, _I, _I, _I, _P, _I, _I, _I])
+    L.pkvo_gather_kv_cache_dequant.restype = _I
+    L.pkvo_gather_kv_cache_dequant.argtypes = [_P, _P, _I, _P] + [_P] * 5 + [_P, _P] + [_I] * 7
     L.pkvo_lse_reduce.restype = None
     L.pkvo_lse_reduce.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I]
 
@@ -186,6 +188,25 @@ def gather_kv_cache(k_cache: np.ndarray, v_cache: np.ndarray, block_tables: np.n
                                     NB, bs, Hkv, D, k_cache.dtype.itemsize)
     if rc:
         raise ValueError("oracle gather: out-of-range block id or context")
+    return k_out, v_out
+
+
+def gather_kv_cache_dequant(qc, block_tables: np.ndarray, context_lens: np.ndarray,
+                            cu_seq_lens: np.ndarray, out_dtype: int = BF16):
+    """K8/V4 codes -> contiguous [sum(ctx), Hkv, D] fp16/bf16 bits (uint16)."""
+    NB, bs, Hkv, D = qc.k_q.shape
+    bt = _c(block_tables, np.int32)
+    cl = _c(context_lens, np.int32)
+    cu = _c(cu_seq_lens, np.int32)
+    total = int(cu[-1])
+    k_out = np.zeros((total, Hkv, D), np.uint16)
+    v_out = np.zeros((total, Hkv, D), np.uint16)
+    rc = lib().pkvo_gather_kv_cache_dequant(
+        _ptr(k_out), _ptr(v_out), out_dtype, _ptr(cu), _ptr(qc.k_q), _ptr(qc.k_scale), _ptr(qc.v_q),
+        _ptr(qc.v_scale), _ptr(qc.v_zero), _ptr(bt), _ptr(cl), bt.shape[0], bt.shape[1], NB, bs, Hkv, D,
+        qc.v_group)
+    if rc:
+        raise ValueError("oracle dequantising gather: out-of-range block id or context")
     return k_out, v_out
 
 

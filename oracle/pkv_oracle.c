@@ -515,3 +515,50 @@ void pkvo_lse_reduce(double *out, const double *part_o, const double *part_m,
         for (int d = 0; d < head_dim; d++) o[d] /= W;
     }
 }
+
+/* Dequantising gather of a K8/V4 cache: every visible token of every sequence
+ * to contiguous [sum(ctx), num_kv_heads, head_dim] rows of out_dtype (OT_F16 or
+ * OT_BF16), logical token t of sequence s going to row cu_seq_lens[s] + t, the
+ * gather of gather_kv_cache [METAL §"Layout matters at the kernel level"] with
+ * the K8/V4 values k = c * s_k and v = c * s_v + z_v [METAL §"The K/V
+ * asymmetry"; MTPLX-2 §"Quantization-Aware Memory Layout"].  Each value is
+ * formed in fp64 (exact for these operands), rounded once to fp32 and then
+ * to out_dtype, both round-to-nearest-even.  Returns -1 on an out-of-range
+ * block id or a context longer than the table, else 0. */
+int pkvo_gather_kv_cache_dequant(uint16_t *k_out, uint16_t *v_out, int out_dtype,
+                                 const int32_t *cu_seq_lens, const int8_t *k_q,
+                                 const uint16_t *k_scale, const uint8_t *v_q,
+                                 const uint16_t *v_scale, const uint16_t *v_zero,
+                                 const int32_t *block_tables, const int32_t *context_lens,
+                                 int num_seqs, int max_blocks, int num_blocks, int block_size,
+                                 int num_kv_heads, int head_dim, int v_group)
+{
+    int H = num_kv_heads, D = head_dim, NG = head_dim / v_group;
+    for (int s = 0; s < num_seqs; s++) {
+        int ctx = context_lens[s];
+        if (ctx > max_blocks * block_size) return -1;
+        for (int t = 0; t < ctx; t++) {
+            int pb = block_tables[(size_t)s * max_blocks + t / block_size];
+            if (pb < 0 || pb >= num_blocks) return -1;
+            int off = t % block_size;
+            for (int h = 0; h < H; h++) {
+                size_t src = ((size_t)pb * block_size + (size_t)off) * H + (size_t)h;
+                size_t meta = ((size_t)pb * H + (size_t)h) * block_size + (size_t)off;
+                size_t dst = (((size_t)cu_seq_lens[s] + (size_t)t) * H + (size_t)h) * D;
+                double sk = pkvo_f16_to_f64(k_scale[meta]);
+                for (int d = 0; d < D; d++) {
+                    double kv = (double)k_q[src * D + d] * sk;
+                    uint8_t byte = v_q[src * (size_t)(D / 2) + (size_t)(d / 2)];
+                    int c = (d & 1) ? (byte >> 4) : (byte & 0x0f);   /* even dim: low nibble */
+                    double sv = pkvo_f16_to_f64(v_scale[meta * NG + d / v_group]);
+                    double zv = pkvo_f16_to_f64(v_zero[meta * NG + d / v_group]);
+                    double vv = (double)c * sv + zv;
+                    float kf = (float)kv, vf = (float)vv;
+                    k_out[dst + d] = out_dtype == OT_F16 ? pkvo_f32_to_f16_rne(kf) : pkvo_f32_to_bf16_rne(kf);
+                    v_out[dst + d] = out_dtype == OT_F16 ? pkvo_f32_to_f16_rne(vf) : pkvo_f32_to_bf16_rne(vf);
+                }
+            }
+        }
+    }
+    return 0;
+}

@@ -165,6 +165,64 @@ def test_k8v4_attention_matches_sdpa_over_independent_dequant():
         np.testing.assert_allclose(got[s], ref.numpy(), rtol=1e-12, atol=1e-13)
 
 
+# ---------------------------------------------------------------- dequantising gather
+
+@pytest.mark.parametrize("out", ["bf16", "f16"])
+def test_dequant_gather_matches_numpy_torch_rounding(out):
+    """Codes unpacked and scaled by numpy from the documented layout, gathered
+    by numpy indexing, rounded fp64 -> fp32 -> out dtype by torch (RNE)."""
+    w = W.build(name="t", seed=9, context_lens=[40, 77, 3, 16], num_heads=8, num_kv_heads=2,
+                head_dim=64, cache="k8v4")
+    cs = oracle_cache_after_step(w)
+    qc = cs["qc"]
+    cu = w.cu_seq_lens().numpy()
+    ko, vo = oracle.gather_kv_cache_dequant(qc, np_i32(w.block_tables), np_i32(w.context_lens), cu,
+                                            oracle.BF16 if out == "bf16" else oracle.F16)
+    NB = qc.num_blocks
+    ks = oracle.f16_bits_to_f64(qc.k_scale).transpose(0, 2, 1)            # [NB, 16, Hkv]
+    k64 = (qc.k_q.astype(np.float64) * ks[..., None]).reshape(NB * 16, 2, 64)
+    vs = np.repeat(oracle.f16_bits_to_f64(qc.v_scale).transpose(0, 2, 1, 3), 32, -1)
+    vz = np.repeat(oracle.f16_bits_to_f64(qc.v_zero).transpose(0, 2, 1, 3), 32, -1)
+    v64 = (_unpack_v(qc) * vs + vz).reshape(NB * 16, 2, 64)
+    tdt = torch.bfloat16 if out == "bf16" else torch.float16
+    table = np_i32(w.block_tables).astype(np.int64)
+    for s in range(w.num_seqs):
+        c = int(w.context_lens[s])
+        t = np.arange(c)
+        slots = table[s][t // 16] * 16 + t % 16
+        for arr, got in ((k64, ko), (v64, vo)):
+            ref = torch.from_numpy(arr[slots].astype(np.float32)).to(tdt).view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(got[cu[s]:cu[s] + c], ref)
+
+
+def test_dequant_gather_of_fresh_quantisation_is_within_half_a_step():
+    w = W.build(name="t", seed=10, context_lens=[33, 64], num_heads=4, num_kv_heads=2, head_dim=128,
+                cache="k8v4", new_tokens="none")
+    cs = oracle_cache_after_step(w)
+    qc = cs["qc"]
+    cu = w.cu_seq_lens().numpy()
+    ko, vo = oracle.gather_kv_cache_dequant(qc, np_i32(w.block_tables), np_i32(w.context_lens), cu, oracle.F16)
+    # history values in slot order -> logical order
+    k_src = oracle.bf16_bits_to_f64(bits(w.k_hist))
+    v_src = oracle.bf16_bits_to_f64(bits(w.v_hist))
+    pos = {int(sl): i for i, sl in enumerate(np_i64(w.slot_hist))}
+    table = np_i32(w.block_tables)
+    for s in range(w.num_seqs):
+        for t in range(int(w.context_lens[s])):
+            i = pos[int(table[s, t // 16]) * 16 + t % 16]
+            blk, off = int(table[s, t // 16]), t % 16
+            kd = oracle.f16_bits_to_f64(ko[cu[s] + t])
+            vd = oracle.f16_bits_to_f64(vo[cu[s] + t])
+            sk = oracle.f16_bits_to_f64(qc.k_scale[blk, :, off])[:, None]
+            sv = np.repeat(oracle.f16_bits_to_f64(qc.v_scale[blk, :, off]), 32, -1)
+            ulp = np.abs(kd) * 2.0 ** -10 + 2.0 ** -24
+            assert np.all(np.abs(kd - k_src[i]) <= 0.5 * sk * (1 + 2.0 ** -9) + ulp)
+            lo = v_src[i].reshape(2, 4, 32).min(-1)
+            vz = oracle.f16_bits_to_f64(qc.v_zero[blk, :, off])
+            slack = np.repeat(np.abs(vz - lo) + 16 * np.abs(sv[:, ::32] - (v_src[i].reshape(2, 4, 32).max(-1) - lo) / 15), 32, -1)
+            assert np.all(np.abs(vd - v_src[i]) <= 0.5 * sv + slack + np.abs(vd) * 2.0 ** -10 + 1e-7)
+
+
 # ---------------------------------------------------------------- bytes model
 
 def test_bytes_model_reproduces_the_pages_worked_example():

@@ -31,6 +31,12 @@ MUTANTS = [
      lambda: TA.test_split_partials_and_reduce_equal_single_pass(32)),
     ("softmax max not subtracted in weights", "double w = exp(x[t - t0] - m);", "double w = exp(x[t - t0]);",
      lambda: TA.test_split_partials_and_reduce_equal_single_pass(16)),
+    ("dequant gather drops the V zero", "double vv = (double)c * sv + zv;", "double vv = (double)c * sv;",
+     lambda: TC.test_dequant_gather_matches_numpy_torch_rounding("bf16")),
+    ("dequant gather reads the neighbour token's scales",
+     "size_t meta = ((size_t)pb * H + (size_t)h) * block_size + (size_t)off;",
+     "size_t meta = ((size_t)pb * H + (size_t)h) * block_size + (size_t)(off ^ 1);",
+     lambda: TC.test_dequant_gather_matches_numpy_torch_rounding("f16")),
     ("window one token short", "if (J->window > 0 && ctx > J->window) lo = ctx - J->window;",
      "if (J->window > 0 && ctx > J->window) lo = ctx - J->window + 1;",
      lambda: TA.test_window_matches_sdpa_over_the_last_tokens(*TA.WINDOW_CASES[0])),
