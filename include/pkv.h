@@ -299,6 +299,23 @@ pkv_status pkv_gather_kv_cache(void *k_out, void *v_out, const int32_t *cu_seq_l
                                const pkv_cache *cache, const pkv_seqs *seqs, uint32_t *err_flags,
                                pkv_stream_t stream);
 
+/*
+ * Dequantising gather of a PKV_CACHE_K8V4 cache: every visible token of every
+ * sequence to contiguous fp16 / bf16 rows, k = code * k_scale and
+ * v = code * v_scale + v_zero [METAL §"The K/V asymmetry"; MTPLX-2
+ * §"Quantization-Aware Memory Layout"], with the gather of pkv_gather_kv_cache.
+ *   out_dtype    PKV_F16 or PKV_BF16.
+ *   cu_seq_lens  int32 [num_seqs + 1] device, as for pkv_gather_kv_cache.
+ *   k_out, v_out [cu[num_seqs], num_kv_heads, head_dim] of out_dtype, caller-owned,
+ *                16-byte aligned.
+ * Each value is formed in fp32 with one rounding (the K product is exact; V is
+ * one fused multiply-add) and rounded to out_dtype to nearest even.  Errors as
+ * for pkv_gather_kv_cache; a non-K8V4 cache is PKV_ERR_INVALID_ARG.
+ */
+pkv_status pkv_gather_kv_cache_dequant(void *k_out, void *v_out, pkv_dtype out_dtype, const int32_t *cu_seq_lens,
+                                       const pkv_cache *cache, const pkv_seqs *seqs, uint32_t *err_flags,
+                                       pkv_stream_t stream);
+
 /* Static English text for a status code. */
 const char *pkv_status_string(pkv_status status);
 

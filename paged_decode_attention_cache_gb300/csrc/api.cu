@@ -537,6 +537,40 @@ pkv_status pkv_gather_kv_cache(void* k_out, void* v_out, const int32_t* cu_seq_l
     return cuda_result(pkv::launch_gather(p, 2, reinterpret_cast<cudaStream_t>(stream)), "gather launch");
 }
 
+pkv_status pkv_gather_kv_cache_dequant(void* k_out, void* v_out, pkv_dtype out_dtype, const int32_t* cu_seq_lens,
+                                       const pkv_cache* cache, const pkv_seqs* seqs, uint32_t* err_flags,
+                                       pkv_stream_t stream) {
+    pkv_status st = check_cache(cache, false);
+    if (st != PKV_OK) return st;
+    if (cache->kind != PKV_CACHE_K8V4) return fail(PKV_ERR_INVALID_ARG, "the dequantising gather needs a K8V4 cache");
+    if (out_dtype != PKV_F16 && out_dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
+    if ((st = check_seqs(seqs)) != PKV_OK) return st;
+    if (seqs->num_seqs == 0) return ok();
+    CHECK_PTR(k_out, "k_out");
+    CHECK_PTR(v_out, "v_out");
+    if (!cu_seq_lens) return fail(PKV_ERR_INVALID_ARG, "cu_seq_lens is NULL");
+    pkv::GatherParams p{};
+    p.k_out = k_out;
+    p.v_out = v_out;
+    p.cu_seq_lens = cu_seq_lens;
+    p.k_cache = cache->k;
+    p.v_cache = cache->v;
+    p.k_scale = cache->k_scale;
+    p.v_scale = cache->v_scale;
+    p.v_zero = cache->v_zero;
+    p.out_dtype = out_dtype;
+    p.block_tables = seqs->block_tables;
+    p.context_lens = seqs->context_lens;
+    p.num_seqs = seqs->num_seqs;
+    p.max_blocks = seqs->max_blocks_per_seq;
+    p.num_blocks = cache->num_blocks;
+    p.num_kv_heads = cache->num_kv_heads;
+    p.head_dim = cache->head_dim;
+    p.err = err_flags;
+    return cuda_result(pkv::launch_gather_dequant(p, reinterpret_cast<cudaStream_t>(stream)),
+                       "dequantising gather launch");
+}
+
 const char* pkv_status_string(pkv_status status) {
     switch (status) {
         case PKV_OK: return "ok";

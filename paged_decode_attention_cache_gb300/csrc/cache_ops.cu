@@ -4,6 +4,8 @@
 //   quantize_kv        K int8 symmetric + V 4-bit asymmetric write path
 // All three are pure data movement bounded by HBM: 16-byte vector accesses,
 // consecutive threads on consecutive 16-byte chunks of a token row.
+#include <type_traits>
+
 #include "pkv_device.cuh"
 #include "pkv_internal.h"
 
@@ -75,6 +77,75 @@ __global__ void __launch_bounds__(kThreads) gather_kernel(GatherParams p, int ch
     for (int i = threadIdx.x; i < n; i += kThreads) {
         kdst[i] = __ldg(ksrc + i);
         vdst[i] = __ldg(vsrc + i);
+    }
+}
+
+// ---------------------------------------------------------------- dequantising gather
+// [metalworking "The KV Cache", §"The K/V asymmetry": k = c * s, v = c * s + z;
+//  gather as above.]  CTA (b, s) expands logical block b of sequence s; a
+// thread takes 8 dims of one (token, kv head): one 8-byte K load, one 4-byte V
+// load, two 16-byte stores.
+template <typename OutT, int D>
+__global__ void __launch_bounds__(kThreads) gather_dequant_kernel(GatherParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    constexpr int NG = D / 32;
+    constexpr int CPT = D / 8;   // 8-dim chunks per (token, kv head)
+    const int s = blockIdx.y, b = blockIdx.x;
+    int ctx = p.context_lens[s];
+    const int cap = p.max_blocks * kBlockSize;
+    if (ctx > cap) {
+        if (b == 0 && threadIdx.x == 0) flag_error(p.err, PKV_DEVERR_CAPACITY);
+        ctx = cap;
+    }
+    const int t0 = b * kBlockSize;
+    if (t0 >= ctx) return;
+    const int ntok = min(kBlockSize, ctx - t0);
+    const int pb = p.block_tables[int64_t(s) * p.max_blocks + b];
+    if (pb < 0 || pb >= p.num_blocks) {
+        if (threadIdx.x == 0) flag_error(p.err, PKV_DEVERR_OOB_BLOCK);
+        return;
+    }
+    const int H = p.num_kv_heads;
+    const int64_t dst_row0 = int64_t(p.cu_seq_lens[s]) + t0;
+    const int n = ntok * H * CPT;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int c = i % CPT, th = i / CPT, h = th % H, tt = th / H;
+        const int64_t row = (int64_t(pb) * kBlockSize + tt) * H + h;          // cache row
+        const int64_t meta = (int64_t(pb) * H + h) * kBlockSize + tt;           // scale index
+        const uint2 kc = __ldg(reinterpret_cast<const uint2*>(static_cast<const int8_t*>(p.k_cache) + row * D) + c);
+        const uint32_t vc = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(p.v_cache) + row * (D / 2)) + c);
+        const float ks = __half2float(__ldg(static_cast<const __half*>(p.k_scale) + meta));
+        const float vs = __half2float(__ldg(static_cast<const __half*>(p.v_scale) + meta * NG + c / 4));
+        const float vz = __half2float(__ldg(static_cast<const __half*>(p.v_zero) + meta * NG + c / 4));
+        float kv[8], vv[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t kw = e < 4 ? kc.x : kc.y;
+            const int code = int(int8_t((kw >> (8 * (e & 3))) & 0xffu));
+            kv[e] = float(code) * ks;                                   // exact
+            vv[e] = fmaf(float((vc >> (4 * e)) & 0xfu), vs, vz);        // one rounding
+        }
+        uint4 ko, vo;
+        uint32_t* kw = &ko.x;
+        uint32_t* vw = &vo.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (sizeof(OutT) == 2 && std::is_same<OutT, __nv_bfloat16>::value) {
+                const __nv_bfloat162 a = __floats2bfloat162_rn(kv[2 * e], kv[2 * e + 1]);
+                const __nv_bfloat162 z = __floats2bfloat162_rn(vv[2 * e], vv[2 * e + 1]);
+                memcpy(kw + e, &a, 4);
+                memcpy(vw + e, &z, 4);
+            } else {
+                const __half2 a = __floats2half2_rn(kv[2 * e], kv[2 * e + 1]);
+                const __half2 z = __floats2half2_rn(vv[2 * e], vv[2 * e + 1]);
+                memcpy(kw + e, &a, 4);
+                memcpy(vw + e, &z, 4);
+            }
+        }
+        const int64_t dst = ((dst_row0 + tt) * H + h) * D + 8 * c;
+        *reinterpret_cast<uint4*>(static_cast<OutT*>(p.k_out) + dst) = ko;
+        *reinterpret_cast<uint4*>(static_cast<OutT*>(p.v_out) + dst) = vo;
     }
 }
 
@@ -193,6 +264,14 @@ cudaError_t launch_gather(const GatherParams& p, int elem_bytes, cudaStream_t st
     const int chunks = p.num_kv_heads * p.head_dim * elem_bytes / 16;
     dim3 grid(p.max_blocks, p.num_seqs);
     return launch_kernel(gather_kernel, grid, dim3(kThreads), 0, stream, p, chunks);
+}
+
+cudaError_t launch_gather_dequant(const GatherParams& p, cudaStream_t stream) {
+    dim3 grid(p.max_blocks, p.num_seqs);
+    const bool bf = p.out_dtype == PKV_BF16;
+    auto* k = p.head_dim == 128 ? (bf ? gather_dequant_kernel<__nv_bfloat16, 128> : gather_dequant_kernel<__half, 128>)
+                                : (bf ? gather_dequant_kernel<__nv_bfloat16, 64> : gather_dequant_kernel<__half, 64>);
+    return launch_kernel(k, grid, dim3(kThreads), 0, stream, p);
 }
 
 cudaError_t launch_quantize_kv(const CacheWriteParams& p, cudaStream_t stream) {

@@ -142,7 +142,13 @@ struct GatherParams {
     int32_t num_kv_heads;
     int32_t head_dim;
     uint32_t* err;
+    // dequantising gather of a K8/V4 cache
+    const void* k_scale;
+    const void* v_scale;
+    const void* v_zero;
+    int32_t out_dtype;
 };
 cudaError_t launch_gather(const GatherParams& p, int elem_bytes, cudaStream_t stream);
+cudaError_t launch_gather_dequant(const GatherParams& p, cudaStream_t stream);
 
 }  // namespace pkv

@@ -86,6 +86,8 @@ def lib():
                                                            _P, _P, _P, _P]
         L.pkv_gather_kv_cache.restype = st
         L.pkv_gather_kv_cache.argtypes = [_P, _P, _P, _P, _P, _P, _P]
+        L.pkv_gather_kv_cache_dequant.restype = st
+        L.pkv_gather_kv_cache_dequant.argtypes = [_P, _P, ctypes.c_int, _P, _P, _P, _P, _P]
         L.pkv_status_string.restype = ctypes.c_char_p
         L.pkv_status_string.argtypes = [ctypes.c_int]
         L.pkv_last_error.restype = ctypes.c_char_p
@@ -277,3 +279,16 @@ def pkv_gather_kv_cache(k_out: torch.Tensor, v_out: torch.Tensor, cu_seq_lens: t
     c, s = cache.c_struct(), seqs.c_struct()
     _check(lib().pkv_gather_kv_cache(_ptr(k_out), _ptr(v_out), _ptr(cu_seq_lens), ctypes.byref(c),
                                      ctypes.byref(s), _err_ptr(err_flags), _stream(stream)))
+
+
+def pkv_gather_kv_cache_dequant(k_out: torch.Tensor, v_out: torch.Tensor, cu_seq_lens: torch.Tensor, cache: Cache,
+                                seqs: Seqs, err_flags=None, stream=None) -> None:
+    """K8/V4 cache -> contiguous fp16/bf16 (the dtype of k_out) K and V rows."""
+    if cu_seq_lens.dtype != torch.int32:
+        raise ValueError("cu_seq_lens must be int32")
+    if k_out.dtype != v_out.dtype or k_out.dtype not in (torch.float16, torch.bfloat16):
+        raise ValueError("k_out / v_out must both be float16 or both bfloat16")
+    c, s = cache.c_struct(), seqs.c_struct()
+    _check(lib().pkv_gather_kv_cache_dequant(_ptr(k_out), _ptr(v_out), _DT[k_out.dtype], _ptr(cu_seq_lens),
+                                             ctypes.byref(c), ctypes.byref(s), _err_ptr(err_flags),
+                                             _stream(stream)))

@@ -106,12 +106,17 @@ class DecodeStep:
         return int(self.k_new.shape[0] > 0) + 1 + int(self.split)
 
     def gather(self, stream=None):
+        """The visible tokens back as contiguous rows (K8/V4: dequantised to the source dtype)."""
         cu = self.w.cu_seq_lens().to(self.seqs.context_lens.device)
         total = int(cu[-1])
-        k_out = torch.empty((total, self.w.num_kv_heads, self.w.head_dim), dtype=self.cache.k.dtype,
-                            device=self.cache.k.device)
+        k8v4 = self.w.cache == "k8v4"
+        dt = _TORCH[self.w.src_dtype] if k8v4 else self.cache.k.dtype
+        k_out = torch.empty((total, self.w.num_kv_heads, self.w.head_dim), dtype=dt, device=self.cache.k.device)
         v_out = torch.empty_like(k_out)
-        ops.pkv_gather_kv_cache(k_out, v_out, cu, self.cache, self.seqs, self.err, stream)
+        if k8v4:
+            ops.pkv_gather_kv_cache_dequant(k_out, v_out, cu, self.cache, self.seqs, self.err, stream)
+        else:
+            ops.pkv_gather_kv_cache(k_out, v_out, cu, self.cache, self.seqs, self.err, stream)
         return k_out, v_out
 
     def error_flags(self) -> int:
