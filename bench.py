@@ -3,9 +3,11 @@
 
 A step is one attention layer's decode step for the whole batch: the new
 tokens' K/V written into the paged cache (reshape_and_cache or quantize_kv),
-attention over every sequence's visible tokens (split-KV phase 1), and the
-log-sum-exp reduce.  The headline workload is the Llama-3-8B-like batch
-(batch 8, 32/8 heads, head_dim 128, bf16, ragged contexts 512..4096).
+attention over every sequence's visible tokens, and the log-sum-exp reduce
+where the schedule splits.  The decode workloads run the step as one launch
+(pkv_decode_step_balanced: write + balanced attention); --schedule picks
+another.  The headline workload is the Llama-3-8B-like batch (batch 8, 32/8
+heads, head_dim 128, bf16, ragged contexts 512..4096).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
@@ -43,13 +45,15 @@ WORKLOADS = {
 }
 DEFAULT_WORKLOAD = "llama3_8b_batch8"
 # schedule of the attention call per workload: the 32K workload is defined with
-# fixed 512-token partitions and a separate reduce; the batched ones use the
-# balanced split with its fused combine; the tiny one is a single pass
-DEFAULT_SCHEDULE = {"tiny_f16": "single", "llama3_8b_batch8": "balanced", "long_context_32k": "split",
-                    "k8v4_batch32": "balanced", "verify_batch256": "balanced",
-                    "sliding_window_b8_w4096": "balanced"}
+# fixed 512-token partitions and a separate reduce; the batched decode ones run
+# the whole step (cache write + balanced attention) as one launch; the verify
+# batch keeps the write as its own launch (measured a little faster); the tiny
+# one is a single pass
+DEFAULT_SCHEDULE = {"tiny_f16": "single", "llama3_8b_batch8": "fused", "long_context_32k": "split",
+                    "k8v4_batch32": "fused", "verify_batch256": "balanced",
+                    "sliding_window_b8_w4096": "fused"}
 KERNEL_NAME = {"single": "pkv_paged_attention", "split": "pkv_paged_attention_split",
-               "balanced": "pkv_paged_attention_balanced"}
+               "balanced": "pkv_paged_attention_balanced", "fused": "pkv_decode_step_balanced"}
 
 
 def parse():
@@ -59,7 +63,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--partition", type=int, default=None, help="split-KV partition size (with --schedule split)")
-    ap.add_argument("--schedule", default=None, choices=["single", "split", "balanced"],
+    ap.add_argument("--schedule", default=None, choices=["single", "split", "balanced", "fused"],
                     help="attention schedule (default: per workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -368,7 +372,9 @@ def main():
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     peak, peak_src = load_peaks()
-    achieved = attn_b / (kern_ms * 1e-3) / 1e9
+    # the fused decode step's kernel also writes the new tokens
+    kern_b = attn_b + (wr_b if schedule == "fused" else 0)
+    achieved = kern_b / (kern_ms * 1e-3) / 1e9
     kernel_name = KERNEL_NAME[schedule]
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": traffic_from_profiles(w.name, kernel_name), "kernel": kernel_name,

@@ -255,6 +255,30 @@ pkv_status pkv_paged_attention_balanced(void *out, pkv_dtype out_dtype, const vo
                                         const pkv_seqs *seqs, void *workspace, size_t workspace_bytes,
                                         uint32_t *err_flags, pkv_stream_t stream);
 
+/*
+ * One decode step in one launch: the cache write of the step's new tokens
+ * (pkv_reshape_and_cache, or pkv_quantize_kv for a K8V4 cache) and the balanced
+ * attention of pkv_paged_attention_balanced, with the same results as those two
+ * calls in that order.  This library's own arrangement of the write and the
+ * read [MLXCEL §"Attention Dispatch and In-Place Decode Writes": the new row is
+ * written into the cache buffer in place]; the pages print no fused call.
+ *   k_new, v_new   [num_tokens, num_kv_heads, head_dim] of src_dtype (the cache
+ *                  dtype for fp16/bf16 caches; PKV_F16 or PKV_BF16 for K8V4).
+ *   slot_mapping   int64 [num_tokens]; < 0 skips the token.
+ *   Token s*q_len + j (j < q_len) is draft j of sequence s.  When its slot is
+ *   the slot of position context_lens[s] - q_len + j, the attention takes that
+ *   row from k_new / v_new (quantised like the write, for K8V4) instead of
+ *   waiting for the write; every other token is only written, and its slot must
+ *   not be one this step's attention reads (else the read races the write).
+ *   Other arguments, workspace and error reporting as for
+ *   pkv_paged_attention_balanced and the write calls.
+ */
+pkv_status pkv_decode_step_balanced(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                    int32_t num_heads, float scale, const pkv_cache *cache, const pkv_seqs *seqs,
+                                    const void *k_new, const void *v_new, pkv_dtype src_dtype,
+                                    const int64_t *slot_mapping, int32_t num_tokens, void *workspace,
+                                    size_t workspace_bytes, uint32_t *err_flags, pkv_stream_t stream);
+
 /* Bytes of device memory the library image reserves for
  * pkv_paged_attention_balanced_noalloc (32 MiB). */
 #define PKV_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -345,14 +345,13 @@ size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int3
     return pkv::balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim);
 }
 
-pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
-                                        int32_t num_heads, float scale, const pkv_cache* cache, const pkv_seqs* seqs,
-                                        void* workspace, size_t workspace_bytes, uint32_t* err_flags,
-                                        pkv_stream_t stream) {
-    pkv::AttnParams p;
-    int gqa = 0;
-    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
-    if (st != PKV_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// Output, workspace and schedule of the balanced entry points (after attn_setup).
+pkv_status balanced_setup(pkv::AttnParams& p, void* out, pkv_dtype out_dtype, const pkv_cache* cache,
+                          const pkv_seqs* seqs, void* workspace, size_t workspace_bytes) {
     CHECK_PTR(out, "out");
     if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
         return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
@@ -381,6 +380,61 @@ pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const vo
     p.mode = pkv::kModeBalanced;
     p.min_chunk = pkv::kMinChunk;
     p.seg_cost = pkv::kSegCost;
+    return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
+                                        int32_t num_heads, float scale, const pkv_cache* cache, const pkv_seqs* seqs,
+                                        void* workspace, size_t workspace_bytes, uint32_t* err_flags,
+                                        pkv_stream_t stream) {
+    pkv::AttnParams p;
+    int gqa = 0;
+    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
+    if (st != PKV_OK) return st;
+    if ((st = balanced_setup(p, out, out_dtype, cache, seqs, workspace, workspace_bytes)) != PKV_OK) return st;
+    if (seqs->num_seqs == 0) return ok();
+    return attn_launch(p, cache, gqa, stream);
+}
+
+pkv_status pkv_decode_step_balanced(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
+                                    int32_t num_heads, float scale, const pkv_cache* cache, const pkv_seqs* seqs,
+                                    const void* k_new, const void* v_new, pkv_dtype src_dtype,
+                                    const int64_t* slot_mapping, int32_t num_tokens, void* workspace,
+                                    size_t workspace_bytes, uint32_t* err_flags, pkv_stream_t stream) {
+    pkv::AttnParams p;
+    int gqa = 0;
+    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
+    if (st != PKV_OK) return st;
+    if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "num_tokens %d", num_tokens);
+    if (cache->kind == PKV_CACHE_K8V4) {
+        if (src_dtype != PKV_F16 && src_dtype != PKV_BF16) return fail(PKV_ERR_INVALID_ARG, "src_dtype %d", src_dtype);
+    } else if (src_dtype != cache_dtype(cache)) {
+        return fail(PKV_ERR_INVALID_ARG, "src_dtype must be the fp16/bf16 cache dtype");
+    }
+    if (num_tokens > 0) {
+        CHECK_PTR(k_new, "k_new");
+        CHECK_PTR(v_new, "v_new");
+        if (!slot_mapping) return fail(PKV_ERR_INVALID_ARG, "slot_mapping is NULL");
+    }
+    if ((st = balanced_setup(p, out, out_dtype, cache, seqs, workspace, workspace_bytes)) != PKV_OK) return st;
+    if (seqs->num_seqs == 0) {
+        // nothing to attend: the write alone
+        if (num_tokens == 0) return ok();
+        return cache->kind == PKV_CACHE_K8V4
+                   ? pkv_quantize_kv(cache, k_new, v_new, src_dtype, slot_mapping, num_tokens, err_flags, stream)
+                   : pkv_reshape_and_cache(cache, k_new, v_new, slot_mapping, num_tokens, err_flags, stream);
+    }
+    p.kc = cache->k;
+    p.vc = cache->v;
+    p.k_new = k_new;
+    p.v_new = v_new;
+    p.slot_mapping = slot_mapping;
+    p.num_new = num_tokens;
+    p.src_dtype = src_dtype;
     return attn_launch(p, cache, gqa, stream);
 }
 

@@ -7,6 +7,7 @@
 #include <type_traits>
 
 #include "pkv_device.cuh"
+#include "pkv_quant.cuh"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -150,21 +151,14 @@ __global__ void __launch_bounds__(kThreads) gather_dequant_kernel(GatherParams p
 }
 
 // ---------------------------------------------------------------- quantize_kv
-// [metalworking "The KV Cache", §"The K/V asymmetry": K stays at 8 bits, V goes
-//  to 4; MTPLX "How MTPLX Manages Memory with KV Caching Strategies", the
-//  quantised write path with per-block scale and zero tensors.]  One warp per
-// (token, kv head).  The fp32 operation sequence is fixed so that codes and
-// scales are reproducible bit for bit: IEEE division (__fdiv_rn), IEEE
-// subtraction (__fsub_rn, never contracted), round-half-even (rintf), and RNE
-// conversion of scales to fp16 before they are used.
+// One warp per (token, kv head); the arithmetic is quantize_row (pkv_quant.cuh).
 template <typename Src, int D>
 __global__ void __launch_bounds__(kThreads) quantize_kernel(CacheWriteParams p) {
     grid_dep_wait();
     grid_dep_launch();
     constexpr int E = D / 32;            // values per lane
-    constexpr int kGroup = 32;           // V group size along head_dim
-    constexpr int NG = D / kGroup;       // groups per row
-    constexpr int LPG = kGroup / E;      // lanes per group
+    constexpr int NG = D / 32;           // V groups per row
+    constexpr int LPG = 32 / E;          // lanes per group
     const int lane = threadIdx.x & 31;
     const int64_t w = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
     const int H = p.num_kv_heads;
@@ -180,68 +174,24 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(CacheWriteParams p) 
     const int64_t blk = slot / kBlockSize;
     const int off = int(slot - blk * kBlockSize);
     const int64_t src = (tok * H + h) * D + lane * E;
-    const uint16_t* ksrc = reinterpret_cast<const uint16_t*>(p.k_new) + src;
-    const uint16_t* vsrc = reinterpret_cast<const uint16_t*>(p.v_new) + src;
-    float k[E], v[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        k[e] = Half16<Src>::to_float(ksrc[e]);
-        v[e] = Half16<Src>::to_float(vsrc[e]);
-    }
-    // K: symmetric int8, one fp16 scale per (token, kv head)
-    float a = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; ++e) a = fmaxf(a, fabsf(k[e]));
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-    const __half s16 = __float2half_rn(__fdiv_rn(a, 127.0f));
-    const float s = __half2float(s16);
-    uint32_t kpack = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float c = (s == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(k[e], s)), -127.f), 127.f);
-        kpack |= (uint32_t(int32_t(c)) & 0xffu) << (8 * e);
-    }
+    const QuantRow<D> q = quantize_row<Src, D>(reinterpret_cast<const uint16_t*>(p.k_new) + src,
+                                               reinterpret_cast<const uint16_t*>(p.v_new) + src);
     const int64_t row = (blk * kBlockSize + off) * H + h;
     const int64_t meta = (blk * H + h) * kBlockSize + off;
     int8_t* kq = reinterpret_cast<int8_t*>(p.k_cache) + row * D + lane * E;
     if constexpr (E == 4)
-        *reinterpret_cast<uint32_t*>(kq) = kpack;
+        *reinterpret_cast<uint32_t*>(kq) = q.kpack;
     else
-        *reinterpret_cast<uint16_t*>(kq) = uint16_t(kpack);
-    if (lane == 0) reinterpret_cast<__half*>(p.k_scale)[meta] = s16;
-
-    // V: asymmetric 4-bit per group of 32 dims, fp16 scale and fp16 zero per group
-    float lo = v[0], hi = v[0];
-#pragma unroll
-    for (int e = 1; e < E; ++e) {
-        lo = fminf(lo, v[e]);
-        hi = fmaxf(hi, v[e]);
-    }
-#pragma unroll
-    for (int o = LPG / 2; o >= 1; o >>= 1) {
-        lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
-        hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
-    }
-    if (lo == 0.f) lo = 0.f;  // a zero minimum is stored as +0
-    const __half vs16 = __float2half_rn(__fdiv_rn(__fsub_rn(hi, lo), 15.0f));
-    const __half vz16 = __float2half_rn(lo);
-    const float vs = __half2float(vs16), vz = __half2float(vz16);
-    uint32_t vpack = 0;
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const float c = (vs == 0.f) ? 0.f : fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(v[e], vz), vs)), 0.f), 15.f);
-        vpack |= uint32_t(c) << (4 * e);  // even dim in the low nibble
-    }
+        *reinterpret_cast<uint16_t*>(kq) = uint16_t(q.kpack);
+    if (lane == 0) reinterpret_cast<__half*>(p.k_scale)[meta] = q.ks;
     uint8_t* vq = reinterpret_cast<uint8_t*>(p.v_cache) + row * (D / 2) + lane * (E / 2);
     if constexpr (E == 4)
-        *reinterpret_cast<uint16_t*>(vq) = uint16_t(vpack);
+        *reinterpret_cast<uint16_t*>(vq) = uint16_t(q.vpack);
     else
-        *vq = uint8_t(vpack);
-    const int g = lane / LPG;
+        *vq = uint8_t(q.vpack);
     if (lane % LPG == 0) {
-        reinterpret_cast<__half*>(p.v_scale)[meta * NG + g] = vs16;
-        reinterpret_cast<__half*>(p.v_zero)[meta * NG + g] = vz16;
+        reinterpret_cast<__half*>(p.v_scale)[meta * NG + lane / LPG] = q.vs;
+        reinterpret_cast<__half*>(p.v_zero)[meta * NG + lane / LPG] = q.vz;
     }
 }
 

@@ -120,6 +120,35 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
+// 16-byte shared-memory copy by explicit shared addresses.
+__device__ __forceinline__ void lds_sts_16(uint32_t dst, uint32_t src) {
+    asm volatile(
+        "{\n\t.reg .b32 a, b, c, d;\n\tld.shared.v4.b32 {a, b, c, d}, [%1];\n\tst.shared.v4.b32 [%0], {a, b, c, d};\n\t}" ::"r"(
+            dst),
+        "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+__device__ __forceinline__ void sts_u8(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.b8 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// 8- and 4-byte global -> shared copies through the load/store path.
+__device__ __forceinline__ void cp_async_8(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Makes the current phase of `bar` also wait for every cp.async this thread has
 // issued so far: the pending arrival count goes up by one now and comes back
 // down when those copies have landed.  Call it before this thread's own arrive

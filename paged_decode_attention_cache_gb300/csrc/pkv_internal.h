@@ -67,6 +67,14 @@ struct AttnParams {
     int32_t stages;     // shared-memory ring depth (a multiple of the consumer warps)
     int32_t min_chunk;  // balanced: fewest 16-token blocks a CTA is given
     int32_t seg_cost;   // balanced: blocks' worth of time one more segment costs a CTA
+    // fused decode step: the cache write of the step's new tokens in the same launch
+    void* kc;                      // the cache's K / V code arrays (written by the fused step)
+    void* vc;
+    const void* k_new;             // [num_new, num_kv_heads, head_dim], src_dtype
+    const void* v_new;
+    const int64_t* slot_mapping;   // [num_new]
+    int32_t num_new;               // 0: attention only
+    int32_t src_dtype;
     float* part_o;      // balanced workspace: [slots, 16, head_dim] unnormalised partial outputs
     float* part_ml;     // [slots, 16, 2] (max, sum) in base-2 units
     int32_t* counters;  // [num_seqs * num_kv_heads] pieces finished per (sequence, kv head)
@@ -89,6 +97,10 @@ bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len);
 bool attention_uses_tensor_cores(int cache_kind, int q_len);
 cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& k_map,
                              const CUtensorMap& v_map, cudaStream_t stream);
+// The fused decode step's kernels (attention_fused.cu); launch_attention calls
+// it when p.num_new > 0.
+cudaError_t launch_attention_fused(AttnParams p, int cache_kind, int gqa, const CUtensorMap& km, const CUtensorMap& vm,
+                                   cudaStream_t stream);
 size_t balanced_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim);
 
 struct ReduceParams {

@@ -81,6 +81,9 @@ def lib():
         L.pkv_paged_attention_balanced.restype = st
         L.pkv_paged_attention_balanced.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
                                                    _P, ctypes.c_size_t, _P, _P]
+        L.pkv_decode_step_balanced.restype = st
+        L.pkv_decode_step_balanced.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
+                                               _P, _P, ctypes.c_int, _P, _I32, _P, ctypes.c_size_t, _P, _P]
         L.pkv_paged_attention_balanced_noalloc.restype = st
         L.pkv_paged_attention_balanced_noalloc.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float,
                                                            _P, _P, _P, _P]
@@ -256,6 +259,23 @@ def pkv_paged_attention_balanced(out: torch.Tensor, q: torch.Tensor, scale: floa
                                               float(scale), ctypes.byref(c), ctypes.byref(s), _ptr(workspace),
                                               int(workspace.numel() * workspace.element_size()),
                                               _err_ptr(err_flags), _stream(stream)))
+    return out
+
+
+def pkv_decode_step_balanced(out: torch.Tensor, q: torch.Tensor, scale: float, cache: Cache, seqs: Seqs,
+                             k_new: torch.Tensor, v_new: torch.Tensor, slot_mapping: torch.Tensor,
+                             workspace: torch.Tensor, err_flags: Optional[torch.Tensor] = None,
+                             stream=None) -> torch.Tensor:
+    """The step's cache write (reshape_and_cache / quantize_kv) and the balanced
+    attention in one launch."""
+    if slot_mapping.dtype != torch.int64:
+        raise ValueError("slot_mapping must be int64")
+    c, s = cache.c_struct(), seqs.c_struct()
+    _check(lib().pkv_decode_step_balanced(_ptr(out), _DT[out.dtype], _ptr(q), _DT[q.dtype], int(q.shape[1]),
+                                          float(scale), ctypes.byref(c), ctypes.byref(s), _ptr(k_new), _ptr(v_new),
+                                          _DT[k_new.dtype], _ptr(slot_mapping), int(slot_mapping.numel()),
+                                          _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+                                          _err_ptr(err_flags), _stream(stream)))
     return out
 
 

@@ -24,7 +24,8 @@ class DecodeStep:
                  out_dtype: Optional[torch.dtype] = None, schedule: Optional[str] = None):
         """schedule: "single" (one CTA per sequence and kv head), "split"
         (fixed partitions of partition_size tokens + LSE reduce) or "balanced"
-        (equal block ranges per SM, combine fused); by default split when the
+        (equal block ranges per SM, combine fused) or "fused" (balanced, with the
+        step's cache write in the same launch); by default split when the
         workload names a partition size, else single."""
         self.w = w
         self.device = device
@@ -32,7 +33,7 @@ class DecodeStep:
         self.partition_size = w.partition_size if partition_size is None else partition_size
         if schedule is None:
             schedule = "split" if self.partition_size > 0 else "single"
-        if schedule not in ("single", "split", "balanced"):
+        if schedule not in ("single", "split", "balanced", "fused"):
             raise ValueError(schedule)
         if schedule != "split":
             self.partition_size = 0
@@ -64,7 +65,7 @@ class DecodeStep:
         if schedule == "split":
             nparts = -(-w.max_blocks * 16 // self.partition_size)
             self.ws = ops.split_workspace(w.num_rows, w.num_heads, w.head_dim, nparts, device=dev)
-        elif schedule == "balanced":
+        elif schedule in ("balanced", "fused"):
             self.bal_ws = ops.balanced_workspace(w.num_seqs, w.num_kv_heads, w.head_dim, device=dev)
 
     @property
@@ -72,7 +73,7 @@ class DecodeStep:
         return self.ws is not None
 
     def write(self, stream=None):
-        if self.k_new.shape[0] == 0:
+        if self.k_new.shape[0] == 0 or self.schedule == "fused":   # fused: written by the attention launch
             return
         if self.w.cache == "k8v4":
             ops.pkv_quantize_kv(self.cache, self.k_new, self.v_new, self.slot_new, self.err, stream)
@@ -88,6 +89,9 @@ class DecodeStep:
         elif self.schedule == "balanced":
             ops.pkv_paged_attention_balanced(self.out, self.q, self.w.scale, self.cache, self.seqs, self.bal_ws,
                                              self.err, stream)
+        elif self.schedule == "fused":
+            ops.pkv_decode_step_balanced(self.out, self.q, self.w.scale, self.cache, self.seqs, self.k_new,
+                                         self.v_new, self.slot_new, self.bal_ws, self.err, stream)
         else:
             ops.pkv_paged_attention(self.out, self.q, self.w.scale, self.cache, self.seqs, self.err, stream)
 
@@ -103,7 +107,7 @@ class DecodeStep:
         return self.out
 
     def launches_per_step(self) -> int:
-        return int(self.k_new.shape[0] > 0) + 1 + int(self.split)
+        return int(self.k_new.shape[0] > 0 and self.schedule != "fused") + 1 + int(self.split)
 
     def gather(self, stream=None):
         """The visible tokens back as contiguous rows (K8/V4: dequantised to the source dtype)."""
