@@ -42,6 +42,7 @@ WORKLOADS = {
     "k8v4_batch32": 4,
     "verify_batch256": 5,
     "sliding_window_b8_w4096": "sliding_window_b8_w4096",
+    "cascade_b32_p2048": "cascade_b32_p2048",
 }
 DEFAULT_WORKLOAD = "llama3_8b_batch8"
 # schedule of the attention call per workload: the 32K workload is defined with
@@ -51,9 +52,10 @@ DEFAULT_WORKLOAD = "llama3_8b_batch8"
 # one is a single pass
 DEFAULT_SCHEDULE = {"tiny_f16": "single", "llama3_8b_batch8": "fused", "long_context_32k": "split",
                     "k8v4_batch32": "fused", "verify_batch256": "balanced",
-                    "sliding_window_b8_w4096": "fused"}
+                    "sliding_window_b8_w4096": "fused", "cascade_b32_p2048": "cascade"}
 KERNEL_NAME = {"single": "pkv_paged_attention", "split": "pkv_paged_attention_split",
-               "balanced": "pkv_paged_attention_balanced", "fused": "pkv_decode_step_balanced"}
+               "balanced": "pkv_paged_attention_balanced", "fused": "pkv_decode_step_balanced",
+               "cascade": "pkv_paged_attention_cascade"}
 
 
 def parse():
@@ -63,7 +65,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--partition", type=int, default=None, help="split-KV partition size (with --schedule split)")
-    ap.add_argument("--schedule", default=None, choices=["single", "split", "balanced", "fused"],
+    ap.add_argument("--schedule", default=None, choices=["single", "split", "balanced", "fused", "cascade"],
                     help="attention schedule (default: per workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -110,11 +112,17 @@ def make_workload(name, device, seed_offset=0, partition=None):
     return w
 
 
-def step_bytes(w):
+def step_bytes(w, cascade_plan=None):
+    """(attention bytes, write bytes) of one step; cascade_plan = (members,
+    item_blocks) counts each item's shared prefix once."""
     from paged_decode_attention_cache_gb300 import bytes_model as BM
     ctx = [int(c) for c in w.context_lens.cpu()]
-    attn = BM.attention_bytes(ctx, w.q_len, w.num_heads, w.num_kv_heads, w.head_dim, w.cache,
-                              sliding_window=w.sliding_window)
+    if cascade_plan is not None:
+        members, blocks = (x.cpu().tolist() for x in cascade_plan)
+        attn = BM.cascade_attention_bytes(ctx, members, blocks, w.num_heads, w.num_kv_heads, w.head_dim, w.cache)
+    else:
+        attn = BM.attention_bytes(ctx, w.q_len, w.num_heads, w.num_kv_heads, w.head_dim, w.cache,
+                                  sliding_window=w.sliding_window)
     wr = BM.write_bytes(int(w.slot_new.numel()), w.num_kv_heads, w.head_dim, w.cache)
     return attn, wr
 
@@ -256,17 +264,19 @@ def main():
     ops.lib()
 
     w = make_workload(args.workload, dev, seed_offset=rank, partition=args.partition)
-    attn_b, wr_b = step_bytes(w)
-    total_b = attn_b + wr_b
-    l2 = getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_BYTES_FALLBACK
-    reps = max(2, math.ceil(3 * l2 / max(1, total_b)))
-    reps = min(reps, 16)
     schedule = args.schedule or DEFAULT_SCHEDULE[args.workload]
     if args.partition is not None and args.schedule is None:
         schedule = "split" if args.partition > 0 else "single"
     if schedule == "split" and w.partition_size <= 0:
         w.partition_size = 512
-    steps_ = [DecodeStep(w, dev, schedule=schedule) for _ in range(reps)]
+    first = DecodeStep(w, dev, schedule=schedule)
+    plan = (first.members, first.item_blocks) if schedule == "cascade" else None
+    attn_b, wr_b = step_bytes(w, plan)
+    total_b = attn_b + wr_b
+    l2 = getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_BYTES_FALLBACK
+    reps = max(2, math.ceil(3 * l2 / max(1, total_b)))
+    reps = min(reps, 16)
+    steps_ = [first] + [DecodeStep(w, dev, schedule=schedule) for _ in range(reps - 1)]
     launches = steps_[0].launches_per_step()
 
     for i in range(max(3, args.warmup)):
@@ -341,24 +351,39 @@ def main():
     e2e = None
     if not (args.no_e2e or args.quick):
         st = steps_[0]
-        host_in = [x.cpu().pin_memory() for x in (st.q, st.k_new, st.v_new, st.slot_new,
-                                                   st.seqs.block_tables, st.seqs.context_lens)]
-        dev_in = [st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens]
+        # the step's inputs packed in one pinned host buffer, copied with one
+        # host-to-device transfer into one device buffer whose views the step
+        # reads; the output comes back with one device-to-host transfer
+        src = [st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens]
+        if schedule == "cascade":
+            src += [st.members, st.item_blocks]
+        offs, total = [], 0
+        for x in src:
+            offs.append(total)
+            total += (x.numel() * x.element_size() + 255) // 256 * 256
+        host_buf = torch.empty(total, dtype=torch.uint8).pin_memory()
+        dev_buf = torch.empty(total, dtype=torch.uint8, device=dev)
+        views = []
+        for x, o in zip(src, offs):
+            n = x.numel() * x.element_size()
+            host_buf[o:o + n].copy_(x.contiguous().view(-1).view(torch.uint8).cpu())
+            views.append(dev_buf[o:o + n].view(x.dtype).view(x.shape))
+        st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens = views[:6]
+        if schedule == "cascade":
+            st.members, st.item_blocks = views[6:]
         host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
-        h2d = sum(x.numel() * x.element_size() for x in host_in)
+        h2d = total
         d2h = host_out.numel() * host_out.element_size()
         Ke = max(10, min(K, 500))
         for _ in range(3):
-            for hsrc, d in zip(host_in, dev_in):
-                d.copy_(hsrc, non_blocking=True)
+            dev_buf.copy_(host_buf, non_blocking=True)
             st.step()
             host_out.copy_(st.out, non_blocking=True)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(Ke):
-            for hsrc, d in zip(host_in, dev_in):
-                d.copy_(hsrc, non_blocking=True)
+            dev_buf.copy_(host_buf, non_blocking=True)
             st.step()
             host_out.copy_(st.out, non_blocking=True)
         e1.record(stream)
@@ -399,6 +424,8 @@ def main():
                    "kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "cache": w.cache,
                    "schedule": schedule, "partition_size": steps_[0].partition_size,
                    "sum_context": int(w.context_lens.sum()),
+                   **({"cascade_items": int(first.members.shape[0]),
+                       "plain_attention_bytes": step_bytes(w)[0]} if schedule == "cascade" else {}),
                    "bytes_per_step": total_b, "parallelism": f"replicas x{ws}",
                    "l2": f"{reps} rotating input replicas, {reps * total_b / 2**20:.0f} MiB touched per cycle "
                          f"vs {l2 / 2**20:.0f} MiB L2"},

@@ -61,6 +61,7 @@ typedef enum pkv_status {
 #define PKV_DEVERR_OOB_SLOT 0x2u   /* a slot_mapping entry >= num_blocks * block_size */
 #define PKV_DEVERR_CAPACITY 0x4u   /* a context longer than its table or partitions */
 #define PKV_DEVERR_TIMEOUT 0x8u    /* a bounded pipeline wait gave up */
+#define PKV_DEVERR_CASCADE 0x10u   /* a cascade member could not join its item (attended whole) */
 
 typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 
@@ -278,6 +279,59 @@ pkv_status pkv_decode_step_balanced(void *out, pkv_dtype out_dtype, const void *
                                     const void *k_new, const void *v_new, pkv_dtype src_dtype,
                                     const int64_t *slot_mapping, int32_t num_tokens, void *workspace,
                                     size_t workspace_bytes, uint32_t *err_flags, pkv_stream_t stream);
+
+/*
+ * Cascade attention over shared whole-page prefixes [MLXCEL §"Paged Decode
+ * Storage and Kernels": opt-in cascade attention for groups that share a
+ * long whole-page prefix].  Same result as pkv_paged_attention (q_len 1, no
+ * sliding window), computed so that an item's shared blocks are read once for
+ * all its members:
+ *   set-up   one thread per (item, member) checks the grouping;
+ *   suffix   split-KV pass over each sequence's tokens after its shared prefix
+ *            (all of them if it is in no item), partials in slots [0, P);
+ *   prefix   split-KV pass over each item's shared blocks, every member of the
+ *            item a query row of the same tiles, partials in slots [P, 2P);
+ *   reduce   the log-sum-exp combination of all 2P slots (pkv_reduce's).
+ * with P = ceil(max_blocks_per_seq * 16 / partition_size).
+ *   members      int32 [num_items, item_width] device: the sequences of each
+ *                item, < 0 pads.  The item's first member lends its block table.
+ *   item_blocks  int32 [num_items] device: leading whole blocks the item shares.
+ *                A member takes part only if its first item_blocks table entries
+ *                equal the first member's, its context covers them and no other
+ *                item holds it; otherwise PKV_DEVERR_CASCADE is flagged and the
+ *                member is attended whole, so the output stays correct.
+ *   item_width   1 .. 16 / (num_heads / num_kv_heads).
+ *   partition_size  positive multiple of 16 (tokens per split-KV partition).
+ *   workspace    pkv_cascade_workspace_bytes(...) bytes, 256-byte aligned.
+ * q_len > 1 or a sliding window: PKV_ERR_UNSUPPORTED.  Every launch goes on `stream`.
+ */
+size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
+                                   int32_t max_blocks_per_seq, int32_t partition_size, int32_t num_items);
+pkv_status pkv_paged_attention_cascade(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                       int32_t num_heads, float scale, const pkv_cache *cache, const pkv_seqs *seqs,
+                                       const int32_t *members, const int32_t *item_blocks, int32_t num_items,
+                                       int32_t item_width, int32_t partition_size, void *workspace,
+                                       size_t workspace_bytes, uint32_t *err_flags, pkv_stream_t stream);
+
+/*
+ * Host-side grouping for pkv_paged_attention_cascade [MLXCEL §"Paged Decode
+ * Storage and Kernels": cascade groups gated by a minimum member count and a
+ * minimum number of shared whole pages].  All pointers are HOST memory:
+ *   block_tables  int32 [num_seqs, max_blocks_per_seq], context_lens int32 [num_seqs]
+ *   members       out int32 [max_items, item_width], -1 pads
+ *   item_blocks   out int32 [max_items]; *num_items = items written.
+ * A sequence's whole pages are its first min(ctx / 16, max_blocks_per_seq)
+ * blocks.  Sequences are sorted by their whole-page block ids; runs of
+ * neighbours sharing >= min_shared_blocks leading blocks form groups of at least
+ * max(min_members, 2), cut into near-equal items of <= item_width members (1..16),
+ * each sharing the common prefix of its members.  Items past max_items are left
+ * out (those sequences are attended whole).  No CUDA call; never fails on
+ * valid pointers.
+ */
+pkv_status pkv_cascade_plan(const int32_t *block_tables, const int32_t *context_lens, int32_t num_seqs,
+                            int32_t max_blocks_per_seq, int32_t min_members, int32_t min_shared_blocks,
+                            int32_t item_width, int32_t max_items, int32_t *members, int32_t *item_blocks,
+                            int32_t *num_items);
 
 /* Bytes of device memory the library image reserves for
  * pkv_paged_attention_balanced_noalloc (32 MiB). */

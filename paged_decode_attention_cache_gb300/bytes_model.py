@@ -53,6 +53,32 @@ def attention_bytes(context_lens, q_len: int, num_heads: int, num_kv_heads: int,
     return kv + qo + tables
 
 
+def cascade_attention_bytes(context_lens, members, item_blocks, num_heads: int, num_kv_heads: int,
+                            head_dim: int, cache: str, q_bytes: int = 2, out_bytes: int = 2,
+                            v_group: int = 32) -> int:
+    """Decode (q_len 1) with cascade items [mlxcel manual "KV Cache", §"Paged
+    Decode Storage and Kernels"]: an item's shared blocks are read once for all
+    its members, every sequence's own tokens after its item's prefix (all of
+    them outside any item) once.  members: rows of sequence indices (< 0 pads),
+    item_blocks: shared whole blocks per item, both as the planner returns them."""
+    kb, vb = row_bytes(cache, head_dim, v_group)
+    start = [0] * len(context_lens)
+    prefix_tokens, prefix_blocks = 0, 0
+    for row, nb in zip(members, item_blocks):
+        nb = int(nb)
+        prefix_tokens += nb * BLOCK_SIZE
+        prefix_blocks += nb
+        for m in row:
+            if int(m) >= 0:
+                start[int(m)] = nb * BLOCK_SIZE
+    suffix_tokens = sum(int(c) - st for c, st in zip(context_lens, start))
+    kv = (prefix_tokens + suffix_tokens) * num_kv_heads * (kb + vb)
+    qo = len(context_lens) * num_heads * head_dim * (q_bytes + out_bytes)
+    tables = 4 * (prefix_blocks + sum(-(-int(c) // BLOCK_SIZE) - st // BLOCK_SIZE
+                                      for c, st in zip(context_lens, start))) + 4 * len(context_lens)
+    return kv + qo + tables
+
+
 def write_bytes(num_tokens: int, num_kv_heads: int, head_dim: int, cache: str, src_bytes: int = 2,
                 v_group: int = 32) -> int:
     """New K/V rows read from the source and written to their slots."""

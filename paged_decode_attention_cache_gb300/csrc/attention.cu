@@ -1,7 +1,7 @@
 // attention.cu -- host side of the attention kernels: which shapes run, the
 // attention-only instantiation of the persistent kernel (attention_impl.cuh)
 // and the balanced workspace size.  The fused decode step's instantiation is
-// in attention_fused.cu.
+// in attention_fused.cu, the cascade passes' in attention_cascade.cu.
 #include "attention_impl.cuh"
 
 namespace pkv {
@@ -13,12 +13,15 @@ bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len) {
     return cache_kind == PKV_CACHE_F16 || cache_kind == PKV_CACHE_BF16;
 }
 
-bool attention_uses_tensor_cores(int cache_kind, int q_len) { return q_len > 1 || cache_kind == PKV_CACHE_K8V4; }
+bool attention_uses_tensor_cores(int cache_kind, int q_len, bool cascade_pass) {
+    return cascade_pass || q_len > 1 || cache_kind == PKV_CACHE_K8V4;
+}
 
 cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& km, const CUtensorMap& vm,
                              cudaStream_t stream) {
+    if (is_cascade_pass(p)) return launch_attention_cascade(p, cache_kind, gqa, km, vm, stream);
     if (p.num_new > 0) return launch_attention_fused(p, cache_kind, gqa, km, vm, stream);
-    return launch_attention_impl<false>(p, cache_kind, gqa, km, vm, stream);
+    return launch_attention_impl<false, false>(p, cache_kind, gqa, km, vm, stream);
 }
 
 size_t balanced_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim) {

@@ -8,7 +8,7 @@ namespace pkv {
 
 cudaError_t launch_attention_fused(AttnParams p, int cache_kind, int gqa, const CUtensorMap& km, const CUtensorMap& vm,
                                    cudaStream_t stream) {
-    return launch_attention_impl<true>(p, cache_kind, gqa, km, vm, stream);
+    return launch_attention_impl<true, false>(p, cache_kind, gqa, km, vm, stream);
 }
 
 }  // namespace pkv

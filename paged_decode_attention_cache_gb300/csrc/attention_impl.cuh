@@ -71,6 +71,31 @@ __host__ __device__ constexpr int ob_idx(int m, int d, int D) { return m * D + (
 
 // ---------------------------------------------------------------- small device helpers
 
+// CASC: the kernel is one pass of cascade attention (the suffix pass reads
+// seq_start, the prefix pass row_map / item_seq); the other kernels compile
+// without those reads.
+
+// First visible token of sequence s: a sliding window keeps the last `window`
+// stored tokens [MTPLX-2 §"Sliding-Window Memory Control"]; the suffix pass of
+// a cascade starts after the sequence's shared prefix.
+template <bool CASC>
+__device__ __forceinline__ int visible_lo(const AttnParams& p, int s, int ctx) {
+    int lo = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+    if constexpr (CASC) {
+        if (p.seq_start) lo = min(max(lo, p.seq_start[s]), ctx);
+    }
+    return lo;
+}
+
+// q / output row of row j of (sequence or cascade item) s; < 0: no row
+template <bool CASC>
+__device__ __forceinline__ int query_row(const AttnParams& p, int s, int j) {
+    if constexpr (CASC) {
+        if (p.row_map) return p.row_map[s * p.q_len + j];
+    }
+    return s * p.q_len + j;
+}
+
 
 template <int W>
 __device__ __forceinline__ int swz(int c, int t) {   // 16-byte chunk c of row t under the W-byte TMA swizzle
@@ -234,9 +259,10 @@ struct CcMath {
         writer = (jl & (LPT / G - 1)) == 0;
     }
 
+    template <bool CASC>
     __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
         const int jl = lane % LPT;
-        lo_ = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+        lo_ = visible_lo<CASC>(p, s, ctx);
         const T* qrow = reinterpret_cast<const T*>(p.q) + (size_t(s) * p.num_heads + kvh * G) * D;
 #pragma unroll
         for (int h = 0; h < G; ++h)
@@ -438,18 +464,21 @@ struct TcMath {
     __device__ __forceinline__ void init(int) {}
 
     // rows g and g+8 of the 16-row tile: row m = head (m / q_len), draft (m % q_len)
+    template <bool CASC>
     __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
         const int g = lane >> 2, tid = lane & 3;
         const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL;
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int m = g + 8 * r;
-            const bool valid = m < M;
-            const int h = valid ? m / QL : 0, j = valid ? m % QL : 0;
-            lim[r] = valid ? max(0, ctx - QL + j + 1) : 0;
-            const size_t qoff = ((size_t(s) * QL + j) * p.num_heads + kvh * G + h) * D;
+            const int h = m < M ? m / QL : 0, j = m < M ? m % QL : 0;
+            const int qr = m < M ? query_row<CASC>(p, s, j) : -1;
+            const bool valid = qr >= 0;
+            // cascade prefix rows see the item's whole context; verify rows are causal
+            lim[r] = valid ? ((CASC && p.cascade) ? ctx : max(0, ctx - QL + j + 1)) : 0;
+            const size_t qoff = (size_t(valid ? qr : 0) * p.num_heads + kvh * G + h) * D;
             const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
-            lo_ = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+            lo_ = visible_lo<CASC>(p, s, ctx);
 #pragma unroll
             for (int kk = 0; kk < NKS; ++kk) {
                 qa[kk][r] = valid ? qw[(qoff + 16 * kk + 2 * tid) / 2] : 0u;
@@ -699,16 +728,18 @@ struct TqMath {
     __device__ __forceinline__ void init(int) {}
 
     // query column n = head (n / q_len), draft (n % q_len)
+    template <bool CASC>
     __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
         const int g = lane >> 2, t = lane & 3;
         const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL;
-        lo_ = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
+        lo_ = visible_lo<CASC>(p, s, ctx);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
             const int n = 8 * nt + g;
-            const bool valid = n < M;
-            const int h = valid ? n / QL : 0, j = valid ? n % QL : 0;
-            const size_t qoff = ((size_t(s) * QL + j) * p.num_heads + kvh * G + h) * D;
+            const int h = n < M ? n / QL : 0, j = n < M ? n % QL : 0;
+            const int qr = n < M ? query_row<CASC>(p, s, j) : -1;
+            const bool valid = qr >= 0;
+            const size_t qoff = (size_t(valid ? qr : 0) * p.num_heads + kvh * G + h) * D;
 #pragma unroll
             for (int kk = 0; kk < NKS; ++kk) {
                 uint32_t lo = 0, hi = 0;
@@ -723,7 +754,9 @@ struct TqMath {
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int n2 = 8 * nt + 2 * t + e;
-                lim[nt][e] = n2 < M ? max(0, ctx - QL + n2 % QL + 1) : 0;
+                const int j2 = n2 % QL;
+                const bool ok2 = n2 < M && query_row<CASC>(p, s, j2) >= 0;
+                lim[nt][e] = ok2 ? ((CASC && p.cascade) ? ctx : max(0, ctx - QL + j2 + 1)) : 0;
                 m_run[nt][e] = -INFINITY;
                 l_part[nt][e] = 0.f;
             }
@@ -929,22 +962,18 @@ __device__ __forceinline__ int seq_ctx(const AttnParams& p, int s) {
     return c < 0 ? 0 : (c > cap ? cap : c);
 }
 
-// First visible token of a sequence: a sliding window keeps the last `window`
-// stored tokens [MTPLX-2 §"Sliding-Window Memory Control"].
-__device__ __forceinline__ int seq_lo(const AttnParams& p, int ctx) {
-    return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
-}
-
-// First unit of a sequence (blocks / partitions wholly before the window are
-// skipped) and its number of units: balanced = blocks; split = partitions.
-__device__ __forceinline__ int seq_first_unit(const AttnParams& p, int ctx) {
-    const int b = seq_lo(p, ctx) / kBS;
+// First unit of a sequence (blocks / partitions wholly before its first visible
+// token are skipped) and its number of units: balanced = blocks; split = partitions.
+template <bool CASC>
+__device__ __forceinline__ int seq_first_unit(const AttnParams& p, int s, int ctx) {
+    const int b = visible_lo<CASC>(p, s, ctx) / kBS;
     return p.mode == kModeBalanced ? b : b / p.partition_blocks;
 }
-__device__ __forceinline__ long long seq_units(const AttnParams& p, int ctx) {
+template <bool CASC>
+__device__ __forceinline__ long long seq_units(const AttnParams& p, int s, int ctx) {
     const int nb = (ctx + kBS - 1) / kBS;
     const int all = p.mode == kModeBalanced ? nb : (nb + p.partition_blocks - 1) / p.partition_blocks;
-    return all - seq_first_unit(p, ctx);
+    return all - seq_first_unit<CASC>(p, s, ctx);
 }
 
 struct Seg {
@@ -957,6 +986,7 @@ struct Seg {
 
 // Iterates this CTA's segments in order.  Every warp runs its own copy; all
 // lanes of a warp hold the same state.
+template <bool CASC>
 struct SegIter {
     long long u, u1;
     int kvh;             // split / balanced: the kv head of this CTA's lane
@@ -973,8 +1003,8 @@ struct SegIter {
         if (s < p.num_seqs) {
             ctx = known_ctx >= 0 ? known_ctx : seq_ctx(p, s);
             nb = (ctx + kBS - 1) / kBS;
-            u_first = seq_first_unit(p, ctx);
-            n = seq_units(p, ctx);
+            u_first = seq_first_unit<CASC>(p, s, ctx);
+            n = seq_units<CASC>(p, s, ctx);
         } else {
             ctx = nb = u_first = 0;
             n = 0;
@@ -989,7 +1019,7 @@ struct SegIter {
             g.kvh = int(u % Hkv);
             g.ctx = seq_ctx(p, g.s);
             g.nb = (g.ctx + kBS - 1) / kBS;
-            g.b0 = seq_lo(p, g.ctx) / kBS;
+            g.b0 = visible_lo<CASC>(p, g.s, g.ctx) / kBS;
             g.b1 = g.nb;
             g.nu = 1;
             g.part = 0;
@@ -1024,7 +1054,7 @@ struct SegIter {
             u += k1 - k;
         } else {
             g.part = u_first + int(k);
-            g.b0 = max(g.part * p.partition_blocks, seq_lo(p, ctx) / kBS);
+            g.b0 = max(g.part * p.partition_blocks, visible_lo<CASC>(p, s, ctx) / kBS);
             g.b1 = min(nb, (g.part + 1) * p.partition_blocks);
             g.pair_start = 0;
             g.cost_base = 0;
@@ -1054,13 +1084,14 @@ struct SeqPos {
 
 // One round of nthr sequences from r0: a block-wide scan of (cost << 32 | units)
 // gives this thread's sequence its first unit and cost position.
+template <bool CASC>
 __device__ __forceinline__ SeqPos plan_round(const AttnParams& p, int r0, long long* red,
                                              unsigned long long& base) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     SeqPos sp;
     sp.s = r0 + threadIdx.x;
     sp.ctx = sp.s < p.num_seqs ? seq_ctx(p, sp.s) : 0;
-    sp.u = sp.s < p.num_seqs ? seq_units(p, sp.ctx) : 0;
+    sp.u = sp.s < p.num_seqs ? seq_units<CASC>(p, sp.s, sp.ctx) : 0;
     const unsigned long long v =
         sp.u > 0 ? ((unsigned long long)(sp.u + p.seg_cost) << 32) | (unsigned long long)sp.u : 0ull;
     unsigned long long incl = v;
@@ -1099,11 +1130,12 @@ __device__ __forceinline__ void plan_resolve(const AttnParams& p, const SeqPos& 
     if (sp.C <= X1 && X1 < c_end) red[13] = sp.U + max(0ll, X1 - sp.C - sc);
 }
 
+template <bool CASC>
 __device__ void cta_plan(const AttnParams& p, int lane_idx, int nlanes, long long* red, int* flag, Plan& pl) {
     const int B = p.num_seqs, nthr = blockDim.x;
     unsigned long long base = 0;
     SeqPos mine{};
-    for (int r0 = 0; r0 < B; r0 += nthr) mine = plan_round(p, r0, red, base);
+    for (int r0 = 0; r0 < B; r0 += nthr) mine = plan_round<CASC>(p, r0, red, base);
     const long long total_u = (long long)(base & 0xffffffffull), total_c = (long long)(base >> 32);
     long long chunk = (total_c + nlanes - 1) / nlanes;
     if (p.mode == kModeBalanced && chunk < p.min_chunk + p.seg_cost) chunk = p.min_chunk + p.seg_cost;
@@ -1121,7 +1153,7 @@ __device__ void cta_plan(const AttnParams& p, int lane_idx, int nlanes, long lon
         plan_resolve(p, mine, X0, X1, red, flag);
     } else {
         base = 0;
-        for (int r0 = 0; r0 < B; r0 += nthr) plan_resolve(p, plan_round(p, r0, red, base), X0, X1, red, flag);
+        for (int r0 = 0; r0 < B; r0 += nthr) plan_resolve(p, plan_round<CASC>(p, r0, red, base), X0, X1, red, flag);
     }
     __syncthreads();
     pl.chunk = chunk;
@@ -1216,7 +1248,7 @@ __device__ void fused_write(const AttnParams& p, int warp, int nwarps, int tid) 
 
 // ---------------------------------------------------------------- the kernel
 
-template <class Math, bool FUSED>
+template <class Math, bool FUSED, bool CASC>
 __global__ void __launch_bounds__((Math::NCW + 1) * 32, 1)
 attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constant__ CUtensorMap v_map,
                  const AttnParams p) {
@@ -1259,6 +1291,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     // so CTAs c .. c+Hkv-1 stream the same blocks' head slices side by side and
     // every 2*Hkv*D-byte token row of a block is read from DRAM at one time.
     const int lane_kvh = blockIdx.x % Hkv, lane_idx = blockIdx.x / Hkv, nlanes = gridDim.x / Hkv;
+    if constexpr (CASC) grid_dep_wait();   // the plan reads what the previous kernel wrote
     Plan pl;
     if (p.mode == kModeSingle) {
         const long long total = (long long)p.num_seqs * Hkv;
@@ -1271,15 +1304,16 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         pl.start0 = 0;
         __syncthreads();
     } else {
-        cta_plan(p, lane_idx, nlanes, red, flag, pl);
+        cta_plan<CASC>(p, lane_idx, nlanes, red, flag, pl);
     }
     const long long chunk = pl.chunk;
-    // Everything above read only the launch's inputs (context lengths), which no
-    // kernel of this library writes; what follows waits for the previous kernel
-    // of the stream before it reads the cache or writes anything.
+    // Except in a cascade pass, everything above read only the launch's inputs
+    // (context lengths), which no kernel of this library writes; what follows
+    // waits for the previous kernel of the stream before it reads the cache or
+    // writes anything.
     if (tid == 0) grid_dep_launch();
 
-    SegIter it;
+    SegIter<CASC> it;
     it.u = pl.u0;
     it.u1 = pl.u0 < pl.u1 ? pl.u1 : pl.u0;
     it.kvh = lane_kvh;
@@ -1302,7 +1336,8 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         bool waited = false;
         Seg sg;
         while (it.next(p, sg)) {
-            const int32_t* bt = p.block_tables + size_t(sg.s) * p.max_blocks;
+            const int bt_seq = (CASC && p.item_seq) ? p.item_seq[sg.s] : sg.s;   // prefix pass: the lending member
+            const int32_t* bt = p.block_tables + size_t(bt_seq) * p.max_blocks;
             const int n = sg.b1 - sg.b0;
             for (int i0 = 0; i0 < n; i0 += grp) {
                 if (lane < grp && i0 + lane < n) {
@@ -1356,7 +1391,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     Seg sg;
     while (it.next(p, sg)) {
         const int n = sg.b1 - sg.b0;
-        mth.begin(p, sg.s, sg.kvh, sg.ctx, lane);
+        mth.template begin<CASC>(p, sg.s, sg.kvh, sg.ctx, lane);
         // Fused step: the warp that will consume a block holding new positions
         // [ctx - q_len, ctx) prefetches those rows from k_new / v_new into its
         // merge buffer (free until the merge) with cp.async, and their slot
@@ -1411,7 +1446,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 const int pos_l = new0 + lane;
                 const int64_t my_slot = lane < QL ? st_slot[lane] : -1;
                 const int my_pb = lane < QL ? st_pb[lane] : -1;
-                const bool in_place = lane < QL && my_slot >= 0 && pos_l >= 0 && pos_l >= seq_lo(p, sg.ctx) &&
+                const bool in_place = lane < QL && my_slot >= 0 && pos_l >= 0 && pos_l >= visible_lo<CASC>(p, sg.s, sg.ctx) &&
                                       my_pb >= 0 && my_pb < p.num_blocks &&
                                       my_slot == int64_t(my_pb) * kBS + pos_l % kBS;
                 const uint32_t mask = __ballot_sync(0xffffffffu, in_place);
@@ -1495,7 +1530,9 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             const int m = (i4 << 2) / D, d = (i4 << 2) - m * D;
             const float L = resL[k], Mx = resM[k];
             const int h = m / QL, jq = m - (m / QL) * QL;
-            const size_t row = size_t(sg.s) * QL + jq;
+            const int qrow = query_row<CASC>(p, sg.s, jq);
+            if (CASC && qrow < 0) continue;   // a cascade item's padding column
+            const size_t row = size_t(qrow);
             const int hg = sg.kvh * G + h;
             if (piece) {
                 reinterpret_cast<float4*>(p.part_o + (size_t(slot) * kMaxRows + m) * D)[d >> 2] = res[k];
@@ -1509,7 +1546,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 const float4 o = live ? make_float4(res[k].x * inv, res[k].y * inv, res[k].z * inv, res[k].w * inv)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 if (p.mode == kModeSplit) {
-                    const size_t pi = (row * H + hg) * p.max_partitions + sg.part;
+                    const size_t pi = (row * H + hg) * p.max_partitions + sg.part + (CASC ? p.part_offset : 0);
                     reinterpret_cast<float4*>(p.tmp_out + pi * D)[d >> 2] = o;
                     if (d == 0) {
                         p.max_logits[pi] = (L > 0.f) ? Mx * kLn2 : -INFINITY;
@@ -1612,7 +1649,7 @@ int smem_bytes(int stages, int M, int QL, int D) {
            (FUSED && !checks_fit(M, QL, D) ? NCW * kCheckBytes : 0) + NCW * M * D * 4 + NCW * Math::SCRATCH + 1024 + 64;
 }
 
-template <class Math, bool FUSED>
+template <class Math, bool FUSED, bool CASC>
 cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t stream) {
     static int num_sms = 0;
     if (num_sms == 0) {
@@ -1631,7 +1668,7 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
     const int smem = smem_bytes<Math, FUSED>(stages, M, p.q_len, p.head_dim);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(attention_kernel<Math, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(attention_kernel<Math, FUSED, CASC>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              kSmemLimit);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -1649,48 +1686,53 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
         if (lane_units < L) L = int(lane_units < 1 ? 1 : lane_units);
         grid = L * p.num_kv_heads;
     }
-    return launch_kernel(attention_kernel<Math, FUSED>, dim3(grid), dim3((Math::NCW + 1) * 32), size_t(smem), stream,
+    return launch_kernel(attention_kernel<Math, FUSED, CASC>, dim3(grid), dim3((Math::NCW + 1) * 32), size_t(smem), stream,
                          km, vm, p);
 }
 
 template <typename T, int D, bool FUSED>
 cudaError_t dispatch_cc(const AttnParams& p, int gqa, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
     switch (gqa) {
-        case 1: return launch_math<CcMath<T, D, 1>, FUSED>(p, km, vm, st);
-        case 2: return launch_math<CcMath<T, D, 2>, FUSED>(p, km, vm, st);
-        case 4: return launch_math<CcMath<T, D, 4>, FUSED>(p, km, vm, st);
-        case 8: return launch_math<CcMath<T, D, 8>, FUSED>(p, km, vm, st);
+        case 1: return launch_math<CcMath<T, D, 1>, FUSED, false>(p, km, vm, st);
+        case 2: return launch_math<CcMath<T, D, 2>, FUSED, false>(p, km, vm, st);
+        case 4: return launch_math<CcMath<T, D, 4>, FUSED, false>(p, km, vm, st);
+        case 8: return launch_math<CcMath<T, D, 8>, FUSED, false>(p, km, vm, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
-// Math for the cache kind, head_dim, group size and q_len, then launch.
-template <bool FUSED>
+// Math for the cache kind, head_dim, group size and q_len, then launch.  Both
+// passes of a cascade take the tensor-core math (the prefix pass has several
+// query rows per kv head; the suffix pass shares its instantiation).
+template <bool FUSED, bool CASC>
 cudaError_t launch_attention_impl(const AttnParams& p, int cache_kind, int gqa, const CUtensorMap& km,
                                   const CUtensorMap& vm, cudaStream_t stream) {
-    if (p.q_len > 1 || cache_kind == PKV_CACHE_K8V4) {
+    if (CASC || p.q_len > 1 || cache_kind == PKV_CACHE_K8V4) {
         switch (cache_kind) {
             case PKV_CACHE_K8V4: {
                 const bool narrow = (p.num_heads / p.num_kv_heads) * p.q_len <= 8;
                 if (p.head_dim == 128)
-                    return narrow ? launch_math<TqMath<128, 1>, FUSED>(p, km, vm, stream)
-                                  : launch_math<TqMath<128, 2>, FUSED>(p, km, vm, stream);
-                return narrow ? launch_math<TqMath<64, 1>, FUSED>(p, km, vm, stream)
-                              : launch_math<TqMath<64, 2>, FUSED>(p, km, vm, stream);
+                    return narrow ? launch_math<TqMath<128, 1>, FUSED, CASC>(p, km, vm, stream)
+                                  : launch_math<TqMath<128, 2>, FUSED, CASC>(p, km, vm, stream);
+                return narrow ? launch_math<TqMath<64, 1>, FUSED, CASC>(p, km, vm, stream)
+                              : launch_math<TqMath<64, 2>, FUSED, CASC>(p, km, vm, stream);
             }
             case PKV_CACHE_BF16:
-                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_BF16, 128>, FUSED>(p, km, vm, stream)
-                                         : launch_math<TcMath<PKV_CACHE_BF16, 64>, FUSED>(p, km, vm, stream);
+                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_BF16, 128>, FUSED, CASC>(p, km, vm, stream)
+                                         : launch_math<TcMath<PKV_CACHE_BF16, 64>, FUSED, CASC>(p, km, vm, stream);
             default:
-                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_F16, 128>, FUSED>(p, km, vm, stream)
-                                         : launch_math<TcMath<PKV_CACHE_F16, 64>, FUSED>(p, km, vm, stream);
+                return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_F16, 128>, FUSED, CASC>(p, km, vm, stream)
+                                         : launch_math<TcMath<PKV_CACHE_F16, 64>, FUSED, CASC>(p, km, vm, stream);
         }
     }
-    if (cache_kind == PKV_CACHE_BF16)
-        return p.head_dim == 128 ? dispatch_cc<__nv_bfloat16, 128, FUSED>(p, gqa, km, vm, stream)
-                                 : dispatch_cc<__nv_bfloat16, 64, FUSED>(p, gqa, km, vm, stream);
-    return p.head_dim == 128 ? dispatch_cc<__half, 128, FUSED>(p, gqa, km, vm, stream)
-                             : dispatch_cc<__half, 64, FUSED>(p, gqa, km, vm, stream);
+    if constexpr (!CASC) {
+        if (cache_kind == PKV_CACHE_BF16)
+            return p.head_dim == 128 ? dispatch_cc<__nv_bfloat16, 128, FUSED>(p, gqa, km, vm, stream)
+                                     : dispatch_cc<__nv_bfloat16, 64, FUSED>(p, gqa, km, vm, stream);
+        return p.head_dim == 128 ? dispatch_cc<__half, 128, FUSED>(p, gqa, km, vm, stream)
+                                 : dispatch_cc<__half, 64, FUSED>(p, gqa, km, vm, stream);
+    }
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace

@@ -75,6 +75,12 @@ struct AttnParams {
     const int64_t* slot_mapping;   // [num_new]
     int32_t num_new;               // 0: attention only
     int32_t src_dtype;
+    // cascade attention over shared prefixes
+    const int32_t* row_map;        // prefix pass: q / output row of (item, member j); < 0: none
+    const int32_t* item_seq;       // prefix pass: the sequence whose block table an item reads
+    const int32_t* seq_start;      // suffix pass: first visible token of each sequence
+    int32_t part_offset;           // added to the partition index of split-mode outputs
+    int32_t cascade;               // 1: prefix pass (every row sees the item's whole context)
     float* part_o;      // balanced workspace: [slots, 16, head_dim] unnormalised partial outputs
     float* part_ml;     // [slots, 16, 2] (max, sum) in base-2 units
     int32_t* counters;  // [num_seqs * num_kv_heads] pieces finished per (sequence, kv head)
@@ -87,6 +93,7 @@ constexpr int kMaxGrid = 1024;  // CTAs of a persistent launch (bounds the balan
 // Balanced schedule: a CTA gets at least kMinChunk blocks, and starting one more
 // (sequence, kv head) segment is charged as kSegCost blocks (its merge and
 // combine take about as long as streaming that many blocks).
+constexpr int kBlockSize = 16;   // token slots per cache block
 constexpr int kMinChunk = 8;
 constexpr int kSegCost = 24;
 
@@ -94,11 +101,15 @@ constexpr int kSegCost = 24;
 // (sequence, kv head, block) work list split into contiguous ranges.
 bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len);
 // Uses the CUDA-core math for fp16/bf16 with q_len 1, tensor cores otherwise.
-bool attention_uses_tensor_cores(int cache_kind, int q_len);
+bool attention_uses_tensor_cores(int cache_kind, int q_len, bool cascade_pass = false);
+// A pass of cascade attention: its own kernel instantiation (attention_cascade.cu)
+inline bool is_cascade_pass(const AttnParams& p) { return p.seq_start != nullptr || p.row_map != nullptr; }
 cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& k_map,
                              const CUtensorMap& v_map, cudaStream_t stream);
 // The fused decode step's kernels (attention_fused.cu); launch_attention calls
 // it when p.num_new > 0.
+cudaError_t launch_attention_cascade(AttnParams p, int cache_kind, int gqa, const CUtensorMap& km,
+                                     const CUtensorMap& vm, cudaStream_t stream);
 cudaError_t launch_attention_fused(AttnParams p, int cache_kind, int gqa, const CUtensorMap& km, const CUtensorMap& vm,
                                    cudaStream_t stream);
 size_t balanced_workspace_bytes(int num_seqs, int num_kv_heads, int head_dim);
@@ -117,8 +128,25 @@ struct ReduceParams {
     int32_t partition_size;
     int32_t max_partitions;
     int32_t window;     // sliding window in tokens, 0 = none
+    int32_t all_parts;  // 1: combine every partition slot (cascade: suffix + prefix)
 };
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream);
+
+// Cascade set-up: item sequences and contexts, each member's suffix start, and
+// the check that a member's table holds its item's shared blocks.
+struct CascadeParams {
+    const int32_t* members;       // [num_items, width], < 0 padding
+    const int32_t* item_blocks;   // [num_items] shared whole blocks
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t num_items, width, num_seqs, max_blocks;
+    int32_t* item_seq;            // out [num_items]
+    int32_t* item_ctx;            // out [num_items]
+    int32_t* item_rows;           // out [num_items, width]: member, or -1 where it is left out
+    int32_t* seq_start;           // out [num_seqs] (zeroed before)
+    uint32_t* err;
+};
+cudaError_t launch_cascade_setup(const CascadeParams& p, cudaStream_t stream);
 
 struct CacheWriteParams {
     void* k_cache;

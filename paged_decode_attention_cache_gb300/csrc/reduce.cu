@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kThreads) lse_reduce_kernel(ReduceParams p) {
     // sliding window: partitions wholly before the last `window` tokens were not written
     const int p_first = (p.window > 0 && ctx > p.window) ? (ctx - p.window) / p.partition_size : 0;
     nparts = nparts > p_first ? nparts - p_first : 0;
+    if (p.all_parts) nparts = p.max_partitions;
     const size_t base = (size_t(r) * p.num_heads + h) * p.max_partitions + p_first;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
@@ -132,6 +133,47 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream) {
     dim3 grid(rows, p.num_heads);
     return launch_kernel(p.head_dim == 128 ? lse_reduce_kernel<128> : lse_reduce_kernel<64>, grid, dim3(kThreads), 0,
                          stream, p);
+}
+
+namespace {
+
+// One thread per (item, member) [MLXCEL §"Paged Decode Storage and Kernels":
+// cascade attention for groups sharing a whole-page prefix].  The item's first
+// member lends its block table; a member takes part in the prefix pass only if
+// its first item_blocks table entries equal that table's, its context covers
+// them, and no other item has claimed it.  A member left out keeps seq_start 0
+// and is attended whole by the suffix pass, so the result stays exact; the
+// error flag tells the caller its grouping was not what it meant.
+__global__ void __launch_bounds__(kThreads) cascade_setup_kernel(CascadeParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int i = blockIdx.x * kThreads + threadIdx.x;
+    if (i >= p.num_items * p.width) return;
+    const int item = i / p.width, j = i - item * p.width;
+    const int s = p.members[i], s0 = p.members[size_t(item) * p.width];
+    const int nb = p.item_blocks[item];
+    const bool item_ok = s0 >= 0 && s0 < p.num_seqs && nb >= 0 && nb <= p.max_blocks;
+    if (j == 0) {
+        p.item_seq[item] = item_ok ? s0 : 0;
+        p.item_ctx[item] = item_ok ? nb * kBlockSize : 0;
+    }
+    int row = -1;
+    if (s >= 0) {
+        bool ok = item_ok && s < p.num_seqs && nb > 0 && p.context_lens[s] >= nb * kBlockSize;
+        for (int b = 0; ok && b < nb; ++b)
+            ok = p.block_tables[size_t(s) * p.max_blocks + b] == p.block_tables[size_t(s0) * p.max_blocks + b];
+        if (ok) ok = atomicCAS(&p.seq_start[s], 0, nb * kBlockSize) == 0;   // one item per sequence
+        if (ok) row = s;
+        else if (nb != 0 || !item_ok) flag_error(p.err, PKV_DEVERR_CASCADE);
+    }
+    p.item_rows[i] = row;
+}
+
+}  // namespace
+
+cudaError_t launch_cascade_setup(const CascadeParams& p, cudaStream_t stream) {
+    const int n = p.num_items * p.width;
+    return launch_kernel(cascade_setup_kernel, dim3((n + kThreads - 1) / kThreads), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace pkv

@@ -87,6 +87,13 @@ def lib():
         L.pkv_paged_attention_balanced_noalloc.restype = st
         L.pkv_paged_attention_balanced_noalloc.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float,
                                                            _P, _P, _P, _P]
+        L.pkv_cascade_workspace_bytes.restype = ctypes.c_size_t
+        L.pkv_cascade_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32]
+        L.pkv_paged_attention_cascade.restype = st
+        L.pkv_paged_attention_cascade.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
+                                                  _P, _P, _I32, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+        L.pkv_cascade_plan.restype = st
+        L.pkv_cascade_plan.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.pkv_gather_kv_cache.restype = st
         L.pkv_gather_kv_cache.argtypes = [_P, _P, _P, _P, _P, _P, _P]
         L.pkv_gather_kv_cache_dequant.restype = st
@@ -289,6 +296,62 @@ def pkv_paged_attention_balanced_noalloc(out: torch.Tensor, q: torch.Tensor, sca
     _check(lib().pkv_paged_attention_balanced_noalloc(_ptr(out), _DT[out.dtype], _ptr(q), _DT[q.dtype],
                                                       int(q.shape[1]), float(scale), ctypes.byref(c),
                                                       ctypes.byref(s), _err_ptr(err_flags), _stream(stream)))
+    return out
+
+
+def pkv_cascade_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, item_width: int,
+                     min_members: int = 2, min_shared_blocks: int = 8):
+    """Group sequences that share whole-page prefixes (host tensors in, host
+    int32 tensors out): returns (members [num_items, item_width], item_blocks
+    [num_items])."""
+    bt = block_tables.detach().to("cpu", torch.int32).contiguous()
+    cl = context_lens.detach().to("cpu", torch.int32).contiguous()
+    n, mb = int(bt.shape[0]), int(bt.shape[1])
+    if cl.numel() != n:
+        raise ValueError("context_lens and block_tables disagree on num_seqs")
+    cap = max(n // 2, 1)
+    members = torch.full((cap, item_width), -1, dtype=torch.int32)
+    blocks = torch.zeros(cap, dtype=torch.int32)
+    count = ctypes.c_int32(0)
+    _check(lib().pkv_cascade_plan(ctypes.c_void_p(bt.data_ptr()), ctypes.c_void_p(cl.data_ptr()), n, mb,
+                                  int(min_members), int(min_shared_blocks), int(item_width), cap,
+                                  ctypes.c_void_p(members.data_ptr()), ctypes.c_void_p(blocks.data_ptr()),
+                                  ctypes.byref(count)))
+    k = int(count.value)
+    return members[:k].clone(), blocks[:k].clone()
+
+
+def pkv_cascade_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_blocks_per_seq: int,
+                                partition_size: int, num_items: int) -> int:
+    return int(lib().pkv_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_blocks_per_seq,
+                                                 partition_size, num_items))
+
+
+def cascade_workspace(num_seqs: int, num_heads: int, head_dim: int, max_blocks_per_seq: int, partition_size: int,
+                      num_items: int, device="cuda") -> torch.Tensor:
+    n = pkv_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_blocks_per_seq, partition_size, num_items)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+
+
+def pkv_paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, scale: float, cache: Cache, seqs: Seqs,
+                                members: torch.Tensor, item_blocks: torch.Tensor, partition_size: int,
+                                workspace: torch.Tensor, err_flags: Optional[torch.Tensor] = None,
+                                stream=None) -> torch.Tensor:
+    """Decode attention with each item's shared prefix read once for all its
+    members (device int32 members [num_items, width], item_blocks [num_items])."""
+    if members.dtype != torch.int32 or item_blocks.dtype != torch.int32:
+        raise ValueError("members / item_blocks must be int32")
+    if members.dim() != 2 or item_blocks.numel() != members.shape[0]:
+        raise ValueError("members must be [num_items, width] and item_blocks [num_items]")
+    c, s = cache.c_struct(), seqs.c_struct()
+    num_items, width = int(members.shape[0]), int(members.shape[1])
+    _check(lib().pkv_paged_attention_cascade(_ptr(out), _DT[out.dtype], _ptr(q), _DT[q.dtype], int(q.shape[1]),
+                                             float(scale), ctypes.byref(c), ctypes.byref(s),
+                                             _ptr(members) if num_items else None,
+                                             _ptr(item_blocks) if num_items else None, num_items,
+                                             max(width, 1), int(partition_size), _ptr(workspace),
+                                             int(workspace.numel() * workspace.element_size()),
+                                             _err_ptr(err_flags), _stream(stream)))
     return out
 
 

@@ -21,21 +21,26 @@ F16_NAN = 0x7E00
 
 class DecodeStep:
     def __init__(self, w: Workload, device: str = "cuda", partition_size: Optional[int] = None,
-                 out_dtype: Optional[torch.dtype] = None, schedule: Optional[str] = None):
+                 out_dtype: Optional[torch.dtype] = None, schedule: Optional[str] = None,
+                 cascade_min_members: int = 2, cascade_min_shared_blocks: int = 8):
         """schedule: "single" (one CTA per sequence and kv head), "split"
         (fixed partitions of partition_size tokens + LSE reduce) or "balanced"
         (equal block ranges per SM, combine fused) or "fused" (balanced, with the
-        step's cache write in the same launch); by default split when the
-        workload names a partition size, else single."""
+        step's cache write in the same launch) or "cascade" (shared whole-page
+        prefixes read once per group, partitions of partition_size tokens, 512
+        by default); by default split when the workload names a partition size,
+        else single."""
         self.w = w
         self.device = device
         dev = torch.device(device)
         self.partition_size = w.partition_size if partition_size is None else partition_size
         if schedule is None:
             schedule = "split" if self.partition_size > 0 else "single"
-        if schedule not in ("single", "split", "balanced", "fused"):
+        if schedule not in ("single", "split", "balanced", "fused", "cascade"):
             raise ValueError(schedule)
-        if schedule != "split":
+        if schedule == "cascade":
+            self.partition_size = self.partition_size or 512
+        elif schedule != "split":
             self.partition_size = 0
         self.schedule = schedule
         self.seqs = ops.Seqs(w.block_tables.to(dev).contiguous(), w.context_lens.to(dev).contiguous(), w.q_len,
@@ -67,6 +72,17 @@ class DecodeStep:
             self.ws = ops.split_workspace(w.num_rows, w.num_heads, w.head_dim, nparts, device=dev)
         elif schedule in ("balanced", "fused"):
             self.bal_ws = ops.balanced_workspace(w.num_seqs, w.num_kv_heads, w.head_dim, device=dev)
+        elif schedule == "cascade":
+            if w.q_len != 1:
+                raise ValueError("cascade attention is for q_len 1 decode")
+            width = max(1, 16 // (w.num_heads // w.num_kv_heads))
+            members, blocks = ops.pkv_cascade_plan(w.block_tables, w.context_lens, width,
+                                                   min_members=cascade_min_members,
+                                                   min_shared_blocks=cascade_min_shared_blocks)
+            self.members = members.to(dev).contiguous()
+            self.item_blocks = blocks.to(dev).contiguous()
+            self.cascade_ws = ops.cascade_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_blocks,
+                                                    self.partition_size, int(members.shape[0]), device=dev)
 
     @property
     def split(self) -> bool:
@@ -89,6 +105,10 @@ class DecodeStep:
         elif self.schedule == "balanced":
             ops.pkv_paged_attention_balanced(self.out, self.q, self.w.scale, self.cache, self.seqs, self.bal_ws,
                                              self.err, stream)
+        elif self.schedule == "cascade":
+            ops.pkv_paged_attention_cascade(self.out, self.q, self.w.scale, self.cache, self.seqs, self.members,
+                                            self.item_blocks, self.partition_size, self.cascade_ws, self.err,
+                                            stream)
         elif self.schedule == "fused":
             ops.pkv_decode_step_balanced(self.out, self.q, self.w.scale, self.cache, self.seqs, self.k_new,
                                          self.v_new, self.slot_new, self.bal_ws, self.err, stream)
@@ -107,7 +127,12 @@ class DecodeStep:
         return self.out
 
     def launches_per_step(self) -> int:
-        return int(self.k_new.shape[0] > 0 and self.schedule != "fused") + 1 + int(self.split)
+        """Kernels of this library one step launches (clearing memsets not counted)."""
+        wr = int(self.k_new.shape[0] > 0 and self.schedule != "fused")
+        if self.schedule == "cascade":
+            items = int(self.members.shape[0]) > 0
+            return wr + 2 + 2 * int(items)   # [set-up], suffix, [prefix], reduce
+        return wr + 1 + int(self.split)
 
     def gather(self, stream=None):
         """The visible tokens back as contiguous rows (K8/V4: dequantised to the source dtype)."""

@@ -104,7 +104,8 @@ def build(*, name: str, seed: int, context_lens: List[int], num_heads: int, num_
           num_blocks: Optional[int] = None, max_blocks: Optional[int] = None,
           new_tokens: str = "tail", value_scale: float = 1.0, spike_frac: float = 0.0,
           spike_scale: float = 8.0, partition_size: int = 0, identity_table: bool = False,
-          device: str = "cpu", scale: Optional[float] = None, sliding_window: int = 0) -> Workload:
+          device: str = "cpu", scale: Optional[float] = None, sliding_window: int = 0,
+          prefix_groups: Optional[List[List[int]]] = None, shared_blocks: int = 0) -> Workload:
     """General seeded workload.
 
     new_tokens:
@@ -120,7 +121,17 @@ def build(*, name: str, seed: int, context_lens: List[int], num_heads: int, num_
     sgen = torch.Generator(device="cpu").manual_seed(seed)
     ctx = torch.tensor(context_lens, dtype=torch.int32)
     nblk = [(-(-c // bs)) for c in context_lens]
-    need = sum(nblk)
+    # shared prefixes: the members of a group point their first shared_blocks
+    # logical blocks at the same physical blocks (one copy of the prompt)
+    group_of = {}
+    for gi, members in enumerate(prefix_groups or []):
+        for m in members:
+            # the step's new token must land past the shared blocks
+            assert context_lens[m] > shared_blocks * bs or (new_tokens != "tail" and
+                                                            context_lens[m] == shared_blocks * bs), \
+                "a member needs tokens past the shared prefix"
+            group_of[m] = gi
+    need = sum(nblk) - sum((len(mm) - 1) * shared_blocks for mm in (prefix_groups or []))
     if num_blocks is None:
         num_blocks = max(need + 1, int(math.ceil(1.1 * need)))
     if max_blocks is None:
@@ -131,9 +142,18 @@ def build(*, name: str, seed: int, context_lens: List[int], num_heads: int, num_
         torch.randperm(num_blocks, generator=sgen).to(torch.int32)
     table = torch.full((B, max_blocks), -1, dtype=torch.int32)
     used = 0
+    group_blocks = {}
     for s in range(B):
-        table[s, :nblk[s]] = perm[used:used + nblk[s]]
-        used += nblk[s]
+        first = 0
+        if s in group_of:
+            gi = group_of[s]
+            if gi not in group_blocks:
+                group_blocks[gi] = perm[used:used + shared_blocks]
+                used += shared_blocks
+            table[s, :shared_blocks] = group_blocks[gi]
+            first = shared_blocks
+        table[s, first:nblk[s]] = perm[used:used + nblk[s] - first]
+        used += nblk[s] - first
     # 2. spike mask over every sequence's logical positions (peaked-softmax workloads)
     spikes = []
     if spike_frac > 0:
@@ -142,14 +162,20 @@ def build(*, name: str, seed: int, context_lens: List[int], num_heads: int, num_
             spikes.append(torch.randperm(context_lens[s], generator=sgen)[:n])
     # history / new split
     hist_pos, new_pos = [], []
+    seen_group = set()
     for s in range(B):
         c = context_lens[s]
+        # a shared prefix is history once (under its group's first member)
+        h0 = 0
+        if s in group_of:
+            h0 = shared_blocks * bs if group_of[s] in seen_group else 0
+            seen_group.add(group_of[s])
         if new_tokens == "tail":
             k = min(q_len, c)
-            hist_pos.append(torch.arange(0, c - k))
+            hist_pos.append(torch.arange(h0, c - k))
             new_pos.append(torch.arange(c - k, c))
         else:
-            hist_pos.append(torch.arange(0, c))
+            hist_pos.append(torch.arange(h0, c))
             new_pos.append(torch.arange(0, 0))
     slot_hist = torch.cat([_slots_of(table[s], hist_pos[s]) for s in range(B)]) if B else \
         torch.zeros(0, dtype=torch.int64)
@@ -271,7 +297,19 @@ def sliding_window_b8_w4096(device="cpu", seed=6, partition_size=512) -> Workloa
                  partition_size=partition_size, sliding_window=4096, device=device)
 
 
+def cascade_b32_p2048(device="cpu", seed=7, partition_size=512) -> Workload:
+    """Shared-prompt decode: batch 32 in 8 groups of 4 whose block tables point at the same
+    128 physical blocks (a 2048-token prompt), each with its own suffix of uniform [16, 1024]
+    tokens; 32/8 heads, head_dim 128, bf16, values N(0,1) * 0.5, one new token per sequence."""
+    g = torch.Generator(device="cpu").manual_seed(seed + 7)
+    ctx = [2048 + x for x in _uniform_ints(g, 32, 16, 1024)]
+    groups = [list(range(4 * i, 4 * i + 4)) for i in range(8)]
+    return build(name="cascade_b32_g4_p2048_h32kv8_d128_bf16", seed=seed, context_lens=ctx, num_heads=32,
+                 num_kv_heads=8, head_dim=128, cache="bf16", max_blocks=256, value_scale=0.5,
+                 partition_size=partition_size, prefix_groups=groups, shared_blocks=128, device=device)
+
+
 CONFIGS = {1: tiny_f16, 2: llama3_8b_batch8, 3: long_context_32k, 4: k8v4_batch32,
            5: verify_batch256}
 # workloads beyond the five configurations (rows ranked next)
-EXTRA = {"sliding_window_b8_w4096": sliding_window_b8_w4096}
+EXTRA = {"sliding_window_b8_w4096": sliding_window_b8_w4096, "cascade_b32_p2048": cascade_b32_p2048}
