@@ -285,14 +285,16 @@ pkv_status pkv_decode_step_balanced(void *out, pkv_dtype out_dtype, const void *
  * Storage and Kernels": opt-in cascade attention for groups that share a
  * long whole-page prefix].  Same result as pkv_paged_attention (q_len 1, no
  * sliding window), computed so that an item's shared blocks are read once for
- * all its members:
- *   set-up   one thread per (item, member) checks the grouping;
- *   suffix   split-KV pass over each sequence's tokens after its shared prefix
- *            (all of them if it is in no item), partials in slots [0, P);
- *   prefix   split-KV pass over each item's shared blocks, every member of the
- *            item a query row of the same tiles, partials in slots [P, 2P);
- *   reduce   the log-sum-exp combination of all 2P slots (pkv_reduce's).
- * with P = ceil(max_blocks_per_seq * 16 / partition_size).
+ * all its members.  Three launches on `stream`:
+ *   set-up     one CTA checks the grouping and lists the work: the items, then
+ *              every sequence from the end of its item's prefix (from 0 if it is
+ *              in no item);
+ *   attention  one balanced pass over that list (the schedule of
+ *              pkv_paged_attention_balanced): an item's blocks are one tile
+ *              stream for all its members, one query row each on tensor cores,
+ *              giving each member a prefix partial; a sequence's own tokens give
+ *              its other partial;
+ *   reduce     the log-sum-exp combination of each row's two partials.
  *   members      int32 [num_items, item_width] device: the sequences of each
  *                item, < 0 pads.  The item's first member lends its block table.
  *   item_blocks  int32 [num_items] device: leading whole blocks the item shares.
@@ -301,17 +303,17 @@ pkv_status pkv_decode_step_balanced(void *out, pkv_dtype out_dtype, const void *
  *                item holds it; otherwise PKV_DEVERR_CASCADE is flagged and the
  *                member is attended whole, so the output stays correct.
  *   item_width   1 .. 16 / (num_heads / num_kv_heads).
- *   partition_size  positive multiple of 16 (tokens per split-KV partition).
- *   workspace    pkv_cascade_workspace_bytes(...) bytes, 256-byte aligned.
- * q_len > 1 or a sliding window: PKV_ERR_UNSUPPORTED.  Every launch goes on `stream`.
+ *   workspace    pkv_cascade_workspace_bytes(...) bytes, 256-byte aligned; it
+ *                needs no clearing.  Calls that share a workspace must not overlap.
+ * q_len > 1 or a sliding window: PKV_ERR_UNSUPPORTED.
  */
-size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                   int32_t max_blocks_per_seq, int32_t partition_size, int32_t num_items);
+size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t num_items, int32_t item_width);
 pkv_status pkv_paged_attention_cascade(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
                                        int32_t num_heads, float scale, const pkv_cache *cache, const pkv_seqs *seqs,
                                        const int32_t *members, const int32_t *item_blocks, int32_t num_items,
-                                       int32_t item_width, int32_t partition_size, void *workspace,
-                                       size_t workspace_bytes, uint32_t *err_flags, pkv_stream_t stream);
+                                       int32_t item_width, void *workspace, size_t workspace_bytes,
+                                       uint32_t *err_flags, pkv_stream_t stream);
 
 /*
  * Host-side grouping for pkv_paged_attention_cascade [MLXCEL §"Paged Decode

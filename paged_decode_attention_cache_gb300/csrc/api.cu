@@ -400,112 +400,113 @@ pkv_status pkv_paged_attention_balanced(void* out, pkv_dtype out_dtype, const vo
     return attn_launch(p, cache, gqa, stream);
 }
 
-size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t head_dim,
-                                   int32_t max_blocks_per_seq, int32_t partition_size, int32_t num_items) {
-    if (num_seqs < 0 || num_heads < 1 || head_dim < 1 || max_blocks_per_seq < 0 || partition_size < 16 ||
-        partition_size % 16 != 0 || num_items < 0)
+size_t pkv_cascade_workspace_bytes(int32_t num_seqs, int32_t num_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t num_items, int32_t item_width) {
+    if (num_seqs < 0 || num_heads < 1 || num_kv_heads < 1 || head_dim < 1 || num_items < 0 || item_width < 1 ||
+        item_width > 16)
         return 0;
-    const size_t slots = 2 * size_t((int64_t(max_blocks_per_seq) * 16 + partition_size - 1) / partition_size);
-    const size_t rhp = size_t(num_seqs) * size_t(num_heads) * (slots ? slots : 1);
-    return align256(rhp * size_t(head_dim) * 4) + 2 * align256(rhp * 4) + align256(size_t(num_seqs) * 4) +
-           2 * align256(size_t(num_items) * 4) + align256(size_t(num_items) * 16 * 4);
+    const size_t rh2 = size_t(num_seqs) * size_t(num_heads) * 2;
+    const size_t list = size_t(num_items) + size_t(num_seqs);
+    return align256(rh2 * size_t(head_dim) * 4) + 2 * align256(rh2 * 4) + 3 * align256(list * 4) +
+           align256(list * size_t(item_width) * 4) + pkv::balanced_workspace_bytes(int(list), num_kv_heads, head_dim);
 }
 
 pkv_status pkv_paged_attention_cascade(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
                                        int32_t num_heads, float scale, const pkv_cache* cache, const pkv_seqs* seqs,
                                        const int32_t* members, const int32_t* item_blocks, int32_t num_items,
-                                       int32_t item_width, int32_t partition_size, void* workspace,
-                                       size_t workspace_bytes, uint32_t* err_flags, pkv_stream_t stream) {
+                                       int32_t item_width, void* workspace, size_t workspace_bytes,
+                                       uint32_t* err_flags, pkv_stream_t stream) {
     pkv::AttnParams p;
     int gqa = 0;
     pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
     if (st != PKV_OK) return st;
     if (seqs->q_len != 1) return fail(PKV_ERR_UNSUPPORTED, "cascade attention is for q_len 1 decode");
     if (seqs->sliding_window != 0) return fail(PKV_ERR_UNSUPPORTED, "cascade attention with a sliding window");
-    if (partition_size < 16 || partition_size % 16 != 0)
-        return fail(PKV_ERR_INVALID_ARG, "partition_size %d is not a positive multiple of 16", partition_size);
     if (num_items < 0) return fail(PKV_ERR_INVALID_ARG, "num_items %d", num_items);
-    if (num_items > 0) {
-        if (item_width < 1 || gqa * item_width > 16)
-            return fail(PKV_ERR_UNSUPPORTED, "item_width %d: group size x item width must be 1..16", item_width);
-        if (!members || !item_blocks) return fail(PKV_ERR_INVALID_ARG, "members / item_blocks is NULL");
-        if (int64_t(num_items) * item_width > INT32_MAX / 2) return fail(PKV_ERR_INVALID_ARG, "too many items");
-        if (!pkv::attention_supported(cache->kind, cache->head_dim, gqa, item_width < 2 ? 2 : item_width))
-            return fail(PKV_ERR_UNSUPPORTED, "no prefix kernel for this shape");
-    }
+    if (item_width < 1 || gqa * item_width > 16)
+        return fail(PKV_ERR_UNSUPPORTED, "item_width %d: group size x item width must be 1..16", item_width);
+    if (num_items > 0 && (!members || !item_blocks)) return fail(PKV_ERR_INVALID_ARG, "members / item_blocks is NULL");
+    if ((int64_t(num_items) + seqs->num_seqs) * item_width > INT32_MAX / 2 ||
+        (int64_t(num_items) + seqs->num_seqs) * cache->num_kv_heads > INT32_MAX / 2)
+        return fail(PKV_ERR_INVALID_ARG, "too many items");
+    if (!pkv::attention_supported(cache->kind, cache->head_dim, gqa, item_width < 2 ? 2 : item_width))
+        return fail(PKV_ERR_UNSUPPORTED, "no cascade kernel for this shape");
+    if (cache->num_kv_heads > pkv::kMaxGrid)
+        return fail(PKV_ERR_UNSUPPORTED, "num_kv_heads %d above %d", cache->num_kv_heads, pkv::kMaxGrid);
     CHECK_PTR(out, "out");
     if (out_dtype != PKV_F16 && out_dtype != PKV_BF16 && out_dtype != PKV_F32)
         return fail(PKV_ERR_INVALID_ARG, "out_dtype %d", out_dtype);
     if (seqs->num_seqs == 0) return ok();
-    const int64_t half = (int64_t(seqs->max_blocks_per_seq) * 16 + partition_size - 1) / partition_size;
-    if (half < 1 || 2 * half > 65535) return fail(PKV_ERR_INVALID_ARG, "%lld partitions", (long long)(2 * half));
-    const size_t need = pkv_cascade_workspace_bytes(seqs->num_seqs, num_heads, cache->head_dim,
-                                                    seqs->max_blocks_per_seq, partition_size, num_items);
+    const size_t need = pkv_cascade_workspace_bytes(seqs->num_seqs, num_heads, cache->num_kv_heads, cache->head_dim,
+                                                    num_items, item_width);
     if (!workspace) return fail(PKV_ERR_INVALID_ARG, "workspace is NULL");
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return fail(PKV_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
     if (workspace_bytes < need)
         return fail(PKV_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
-    const int slots = int(2 * half);
-    const size_t rhp = size_t(seqs->num_seqs) * size_t(num_heads) * size_t(slots);
+    const size_t rh2 = size_t(seqs->num_seqs) * size_t(num_heads) * 2;
+    const size_t list = size_t(num_items) + size_t(seqs->num_seqs);
+    const size_t pairs = list * size_t(cache->num_kv_heads);
+    const size_t piece_slots = size_t(pkv::kMaxGrid) + pairs;
     uint8_t* w = static_cast<uint8_t*>(workspace);
     float* tmp_out = reinterpret_cast<float*>(w);
-    w += align256(rhp * size_t(cache->head_dim) * 4);
+    w += align256(rh2 * size_t(cache->head_dim) * 4);
     float* max_logits = reinterpret_cast<float*>(w);
-    w += align256(rhp * 4);
+    w += align256(rh2 * 4);
     float* exp_sums = reinterpret_cast<float*>(w);
-    w += align256(rhp * 4);
-    int32_t* seq_start = reinterpret_cast<int32_t*>(w);
-    w += align256(size_t(seqs->num_seqs) * 4);
-    int32_t* item_seq = reinterpret_cast<int32_t*>(w);
-    w += align256(size_t(num_items) * 4);
-    int32_t* item_ctx = reinterpret_cast<int32_t*>(w);
-    w += align256(size_t(num_items) * 4);
-    int32_t* item_rows = reinterpret_cast<int32_t*>(w);
+    w += align256(rh2 * 4);
+    int32_t* list_ctx = reinterpret_cast<int32_t*>(w);
+    w += align256(list * 4);
+    int32_t* list_seq = reinterpret_cast<int32_t*>(w);
+    w += align256(list * 4);
+    int32_t* list_start = reinterpret_cast<int32_t*>(w);
+    w += align256(list * 4);
+    int32_t* list_rows = reinterpret_cast<int32_t*>(w);
+    w += align256(list * size_t(item_width) * 4);
+    p.part_o = reinterpret_cast<float*>(w);
+    w += align256(piece_slots * 16 * size_t(cache->head_dim) * 4);
+    p.part_ml = reinterpret_cast<float*>(w);
+    w += align256(piece_slots * 16 * 2 * 4);
+    p.counters = reinterpret_cast<int32_t*>(w);
     cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-    // partitions a pass does not write (before a suffix, past a prefix) carry no weight
-    cudaError_t e = cudaMemsetAsync(exp_sums, 0, rhp * 4, cs);
-    if (e == cudaSuccess) e = cudaMemsetAsync(seq_start, 0, size_t(seqs->num_seqs) * 4, cs);
-    if (e != cudaSuccess) return cuda_result(e, "clearing the cascade workspace");
-    if (num_items > 0) {
-        pkv::CascadeParams c{};
-        c.members = members;
-        c.item_blocks = item_blocks;
-        c.block_tables = seqs->block_tables;
-        c.context_lens = seqs->context_lens;
-        c.num_items = num_items;
-        c.width = item_width;
-        c.num_seqs = seqs->num_seqs;
-        c.max_blocks = seqs->max_blocks_per_seq;
-        c.item_seq = item_seq;
-        c.item_ctx = item_ctx;
-        c.item_rows = item_rows;
-        c.seq_start = seq_start;
-        c.err = err_flags;
-        if ((e = pkv::launch_cascade_setup(c, cs)) != cudaSuccess) return cuda_result(e, "cascade set-up launch");
-    }
-    // suffix pass: each sequence's own tokens from seq_start on, slots [0, half)
+
+    pkv::CascadeParams c{};
+    c.members = members;
+    c.item_blocks = item_blocks;
+    c.block_tables = seqs->block_tables;
+    c.context_lens = seqs->context_lens;
+    c.num_items = num_items;
+    c.width = item_width;
+    c.num_seqs = seqs->num_seqs;
+    c.max_blocks = seqs->max_blocks_per_seq;
+    c.list_ctx = list_ctx;
+    c.list_seq = list_seq;
+    c.list_start = list_start;
+    c.list_rows = list_rows;
+    c.counters = p.counters;
+    c.num_counters = int32_t(pairs);
+    c.err = err_flags;
+    cudaError_t e = pkv::launch_cascade_setup(c, cs);
+    if (e != cudaSuccess) return cuda_result(e, "cascade set-up launch");
+    // one balanced pass over the list: an item's combined partial goes to slot 1
+    // of its members' rows, a sequence's own to slot 0
     p.tmp_out = tmp_out;
     p.max_logits = max_logits;
     p.exp_sums = exp_sums;
-    p.partition_blocks = partition_size / 16;
-    p.max_partitions = slots;
-    p.mode = pkv::kModeSplit;
-    p.seq_start = seq_start;
+    p.partition_blocks = seqs->max_blocks_per_seq;
+    p.max_partitions = 2;
+    p.mode = pkv::kModeBalanced;
+    p.min_chunk = pkv::kMinChunk;
+    p.seg_cost = pkv::kSegCost;
+    p.num_seqs = int32_t(list);
+    p.q_len = item_width;
+    p.context_lens = list_ctx;
+    p.item_seq = list_seq;
+    p.seq_start = list_start;
+    p.row_map = list_rows;
+    p.num_items = num_items;
+    p.part_offset = 1;
     if ((st = attn_launch(p, cache, gqa, stream)) != PKV_OK) return st;
-    // prefix pass: every item's shared blocks once for all its members, slots [half, 2 half)
-    if (num_items > 0) {
-        pkv::AttnParams pp = p;
-        pp.seq_start = nullptr;
-        pp.num_seqs = num_items;
-        pp.q_len = item_width;
-        pp.context_lens = item_ctx;
-        pp.item_seq = item_seq;
-        pp.row_map = item_rows;
-        pp.cascade = 1;
-        pp.part_offset = int32_t(half);
-        if ((st = attn_launch(pp, cache, gqa, stream)) != PKV_OK) return st;
-    }
     pkv::ReduceParams r{};
     r.out = out;
     r.out_dtype = out_dtype;
@@ -517,9 +518,9 @@ pkv_status pkv_paged_attention_cascade(void* out, pkv_dtype out_dtype, const voi
     r.q_len = 1;
     r.num_heads = num_heads;
     r.head_dim = cache->head_dim;
-    r.partition_size = partition_size;
-    r.max_partitions = slots;
-    r.all_parts = 1;
+    r.partition_size = 16;
+    r.max_partitions = 2;
+    r.seq_start = list_start + num_items;
     return cuda_result(pkv::launch_reduce(r, cs), "cascade reduce launch");
 }
 

@@ -71,28 +71,24 @@ __host__ __device__ constexpr int ob_idx(int m, int d, int D) { return m * D + (
 
 // ---------------------------------------------------------------- small device helpers
 
-// CASC: the kernel is one pass of cascade attention (the suffix pass reads
-// seq_start, the prefix pass row_map / item_seq); the other kernels compile
-// without those reads.
+// CASC: the kernel runs cascade attention's pass over its list (the items'
+// shared prefixes, then every sequence from its seq_start on), where entry s
+// reads the table of item_seq[s] for the query rows row_map[s * q_len + j];
+// the other kernels compile without those reads.
 
-// First visible token of sequence s: a sliding window keeps the last `window`
-// stored tokens [MTPLX-2 §"Sliding-Window Memory Control"]; the suffix pass of
-// a cascade starts after the sequence's shared prefix.
+// First visible token of list entry s: a sliding window keeps the last `window`
+// stored tokens [MTPLX-2 §"Sliding-Window Memory Control"]; a cascade entry
+// starts at its seq_start (past its item's shared prefix).
 template <bool CASC>
 __device__ __forceinline__ int visible_lo(const AttnParams& p, int s, int ctx) {
-    int lo = (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
-    if constexpr (CASC) {
-        if (p.seq_start) lo = min(max(lo, p.seq_start[s]), ctx);
-    }
-    return lo;
+    if constexpr (CASC) return min(max(p.seq_start[s], 0), ctx);
+    return (p.window > 0 && ctx > p.window) ? ctx - p.window : 0;
 }
 
-// q / output row of row j of (sequence or cascade item) s; < 0: no row
+// q / output row of row j of list entry s; < 0: no row
 template <bool CASC>
 __device__ __forceinline__ int query_row(const AttnParams& p, int s, int j) {
-    if constexpr (CASC) {
-        if (p.row_map) return p.row_map[s * p.q_len + j];
-    }
+    if constexpr (CASC) return p.row_map[s * p.q_len + j];
     return s * p.q_len + j;
 }
 
@@ -474,8 +470,8 @@ struct TcMath {
             const int h = m < M ? m / QL : 0, j = m < M ? m % QL : 0;
             const int qr = m < M ? query_row<CASC>(p, s, j) : -1;
             const bool valid = qr >= 0;
-            // cascade prefix rows see the item's whole context; verify rows are causal
-            lim[r] = valid ? ((CASC && p.cascade) ? ctx : max(0, ctx - QL + j + 1)) : 0;
+            // a cascade row (one decode query) sees the entry's whole context; verify rows are causal
+            lim[r] = valid ? (CASC ? ctx : max(0, ctx - QL + j + 1)) : 0;
             const size_t qoff = (size_t(valid ? qr : 0) * p.num_heads + kvh * G + h) * D;
             const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
             lo_ = visible_lo<CASC>(p, s, ctx);
@@ -756,7 +752,7 @@ struct TqMath {
                 const int n2 = 8 * nt + 2 * t + e;
                 const int j2 = n2 % QL;
                 const bool ok2 = n2 < M && query_row<CASC>(p, s, j2) >= 0;
-                lim[nt][e] = ok2 ? ((CASC && p.cascade) ? ctx : max(0, ctx - QL + j2 + 1)) : 0;
+                lim[nt][e] = ok2 ? (CASC ? ctx : max(0, ctx - QL + j2 + 1)) : 0;
                 m_run[nt][e] = -INFINITY;
                 l_part[nt][e] = 0.f;
             }
@@ -1336,7 +1332,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         bool waited = false;
         Seg sg;
         while (it.next(p, sg)) {
-            const int bt_seq = (CASC && p.item_seq) ? p.item_seq[sg.s] : sg.s;   // prefix pass: the lending member
+            const int bt_seq = CASC ? p.item_seq[sg.s] : sg.s;   // cascade: an item reads its lending member's table
             const int32_t* bt = p.block_tables + size_t(bt_seq) * p.max_blocks;
             const int n = sg.b1 - sg.b0;
             for (int i0 = 0; i0 < n; i0 += grp) {
@@ -1378,10 +1374,23 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     // so no CTA has to wait for another's write
     if constexpr (FUSED) fused_write<Math::kQ8, Math::kD>(p, warp, NCW, tid);
     // balanced mode: sequences with nothing visible still get their zero rows
-    if (p.mode == kModeBalanced)
-        for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x)
-            if (seq_ctx(p, s) == 0)
-                for (int i = tid; i < QL * H * D; i += CT) store_out(p.out, p.out_dtype, size_t(s) * QL * H * D + i, 0.f);
+    // (cascade: an empty partial in the sequence's own slot)
+    if (p.mode == kModeBalanced) {
+        if constexpr (CASC) {
+            for (int s = p.num_items + blockIdx.x; s < p.num_seqs; s += gridDim.x)
+                if (seq_units<CASC>(p, s, seq_ctx(p, s)) == 0)
+                    for (int h = tid; h < H; h += CT) {
+                        const size_t pi = (size_t(query_row<CASC>(p, s, 0)) * H + h) * p.max_partitions;
+                        p.max_logits[pi] = -INFINITY;
+                        p.exp_sums[pi] = 0.f;
+                    }
+        } else {
+            for (int s = blockIdx.x; s < p.num_seqs; s += gridDim.x)
+                if (seq_ctx(p, s) == 0)
+                    for (int i = tid; i < QL * H * D; i += CT)
+                        store_out(p.out, p.out_dtype, size_t(s) * QL * H * D + i, 0.f);
+        }
+    }
 
     Math mth;
     mth.init(lane);
@@ -1545,8 +1554,10 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 const float inv = live ? 1.f / L : 0.f;
                 const float4 o = live ? make_float4(res[k].x * inv, res[k].y * inv, res[k].z * inv, res[k].w * inv)
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                if (p.mode == kModeSplit) {
-                    const size_t pi = (row * H + hg) * p.max_partitions + sg.part + (CASC ? p.part_offset : 0);
+                if (CASC || p.mode == kModeSplit) {
+                    // cascade: an item's partial goes to its members' slot part_offset
+                    const int slot_p = sg.part + ((CASC && sg.s < p.num_items) ? p.part_offset : 0);
+                    const size_t pi = (row * H + hg) * p.max_partitions + slot_p;
                     reinterpret_cast<float4*>(p.tmp_out + pi * D)[d >> 2] = o;
                     if (d == 0) {
                         p.max_logits[pi] = (L > 0.f) ? Mx * kLn2 : -INFINITY;
@@ -1631,9 +1642,22 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                     const bool live = L > 0.f;
                     const float inv = live ? 1.f / L : 0.f;
                     const int h = m / QL, jq = m - (m / QL) * QL;
-                    store_out4(p.out, p.out_dtype, ((size_t(sg.s) * QL + jq) * H + sg.kvh * G + h) * D + d,
-                               live ? make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f));
+                    const float4 o = live ? make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv)
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                    if constexpr (CASC) {
+                        // the pair's combined partial into its slot (items: part_offset)
+                        const int qrow = query_row<CASC>(p, sg.s, jq);
+                        if (qrow < 0) continue;
+                        const size_t pi = (size_t(qrow) * H + sg.kvh * G + h) * p.max_partitions +
+                                          (sg.s < p.num_items ? p.part_offset : 0);
+                        reinterpret_cast<float4*>(p.tmp_out + pi * D)[d >> 2] = o;
+                        if (d == 0) {
+                            p.max_logits[pi] = live ? Mr[k] * kLn2 : -INFINITY;
+                            p.exp_sums[pi] = L;
+                        }
+                    } else {
+                        store_out4(p.out, p.out_dtype, ((size_t(sg.s) * QL + jq) * H + sg.kvh * G + h) * D + d, o);
+                    }
                 }
                 if (tid == 0) p.counters[pair] = 0;   // ready for the next launch
             }
@@ -1701,9 +1725,9 @@ cudaError_t dispatch_cc(const AttnParams& p, int gqa, const CUtensorMap& km, con
     }
 }
 
-// Math for the cache kind, head_dim, group size and q_len, then launch.  Both
-// passes of a cascade take the tensor-core math (the prefix pass has several
-// query rows per kv head; the suffix pass shares its instantiation).
+// Math for the cache kind, head_dim, group size and q_len, then launch.  The
+// cascade pass takes the tensor-core math (an item has several query rows per
+// kv head; the sequences' own entries share its instantiation).
 template <bool FUSED, bool CASC>
 cudaError_t launch_attention_impl(const AttnParams& p, int cache_kind, int gqa, const CUtensorMap& km,
                                   const CUtensorMap& vm, cudaStream_t stream) {

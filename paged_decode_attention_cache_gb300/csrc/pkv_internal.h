@@ -75,12 +75,15 @@ struct AttnParams {
     const int64_t* slot_mapping;   // [num_new]
     int32_t num_new;               // 0: attention only
     int32_t src_dtype;
-    // cascade attention over shared prefixes
-    const int32_t* row_map;        // prefix pass: q / output row of (item, member j); < 0: none
-    const int32_t* item_seq;       // prefix pass: the sequence whose block table an item reads
-    const int32_t* seq_start;      // suffix pass: first visible token of each sequence
-    int32_t part_offset;           // added to the partition index of split-mode outputs
-    int32_t cascade;               // 1: prefix pass (every row sees the item's whole context)
+    // cascade attention [one pass over a list of num_items items, then the
+    // sequences]: entry s of the list reads the block table of sequence
+    // item_seq[s] from token seq_start[s] on, for query rows row_map[s * q_len + j]
+    // (< 0: none); an item's partials go to partition part_offset + part
+    const int32_t* row_map;
+    const int32_t* item_seq;
+    const int32_t* seq_start;
+    int32_t num_items;
+    int32_t part_offset;
     float* part_o;      // balanced workspace: [slots, 16, head_dim] unnormalised partial outputs
     float* part_ml;     // [slots, 16, 2] (max, sum) in base-2 units
     int32_t* counters;  // [num_seqs * num_kv_heads] pieces finished per (sequence, kv head)
@@ -128,22 +131,28 @@ struct ReduceParams {
     int32_t partition_size;
     int32_t max_partitions;
     int32_t window;     // sliding window in tokens, 0 = none
-    int32_t all_parts;  // 1: combine every partition slot (cascade: suffix + prefix)
+    // cascade (max_partitions 2): slot 0 of row s holds its own partial, slot 1
+    // its item's when seq_start[s] > 0; null: not a cascade
+    const int32_t* seq_start;
 };
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream);
 
-// Cascade set-up: item sequences and contexts, each member's suffix start, and
-// the check that a member's table holds its item's shared blocks.
+// Cascade set-up (one CTA): the pass's list -- items first, then the sequences
+// -- with each entry's context, lending table, first token and query rows; a
+// member joins its item only if its table holds the item's shared blocks, its
+// context covers them and no other item holds it (else PKV_DEVERR_CASCADE).
 struct CascadeParams {
     const int32_t* members;       // [num_items, width], < 0 padding
     const int32_t* item_blocks;   // [num_items] shared whole blocks
     const int32_t* block_tables;
     const int32_t* context_lens;
     int32_t num_items, width, num_seqs, max_blocks;
-    int32_t* item_seq;            // out [num_items]
-    int32_t* item_ctx;            // out [num_items]
-    int32_t* item_rows;           // out [num_items, width]: member, or -1 where it is left out
-    int32_t* seq_start;           // out [num_seqs] (zeroed before)
+    int32_t* list_ctx;            // out [num_items + num_seqs]
+    int32_t* list_seq;            // out [num_items + num_seqs]: the table each entry reads
+    int32_t* list_start;          // out [num_items + num_seqs]: first visible token
+    int32_t* list_rows;           // out [num_items + num_seqs, width]: query rows, -1 none
+    int32_t* counters;            // the balanced pass's piece counters, cleared here
+    int32_t num_counters;
     uint32_t* err;
 };
 cudaError_t launch_cascade_setup(const CascadeParams& p, cudaStream_t stream);

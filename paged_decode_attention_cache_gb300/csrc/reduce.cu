@@ -40,8 +40,9 @@ __global__ void __launch_bounds__(kThreads) lse_reduce_kernel(ReduceParams p) {
     // sliding window: partitions wholly before the last `window` tokens were not written
     const int p_first = (p.window > 0 && ctx > p.window) ? (ctx - p.window) / p.partition_size : 0;
     nparts = nparts > p_first ? nparts - p_first : 0;
-    if (p.all_parts) nparts = p.max_partitions;
     const size_t base = (size_t(r) * p.num_heads + h) * p.max_partitions + p_first;
+    // cascade: the row's own partial (slot 0), then its item's (slot 1) if it has one
+    if (p.seq_start) nparts = p.seq_start[s] > 0 ? 2 : 1;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     // M = max over partitions with weight
@@ -137,43 +138,65 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t stream) {
 
 namespace {
 
-// One thread per (item, member) [MLXCEL §"Paged Decode Storage and Kernels":
-// cascade attention for groups sharing a whole-page prefix].  The item's first
-// member lends its block table; a member takes part in the prefix pass only if
-// its first item_blocks table entries equal that table's, its context covers
-// them, and no other item has claimed it.  A member left out keeps seq_start 0
-// and is attended whole by the suffix pass, so the result stays exact; the
-// error flag tells the caller its grouping was not what it meant.
-__global__ void __launch_bounds__(kThreads) cascade_setup_kernel(CascadeParams p) {
+// Cascade set-up [mlxcel manual "KV Cache", §"Paged Decode Storage and
+// Kernels": cascade attention for groups sharing a whole-page prefix], one CTA:
+// (1) every sequence gets its list entry (whole context, own table, start 0, one
+//     query row); (2) one warp per (item, member) checks that the member's first
+//     item_blocks table entries equal the lending (first) member's and that its
+//     context covers them, then claims the member for the item.  A member left
+//     out keeps start 0 and is attended whole by its own entry, so the result
+//     stays exact; the error flag tells the caller its grouping was not what it
+//     meant.
+constexpr int kSetupThreads = 1024;
+
+__global__ void __launch_bounds__(kSetupThreads) cascade_setup_kernel(CascadeParams p) {
     grid_dep_wait();
     grid_dep_launch();
-    const int i = blockIdx.x * kThreads + threadIdx.x;
-    if (i >= p.num_items * p.width) return;
-    const int item = i / p.width, j = i - item * p.width;
-    const int s = p.members[i], s0 = p.members[size_t(item) * p.width];
-    const int nb = p.item_blocks[item];
-    const bool item_ok = s0 >= 0 && s0 < p.num_seqs && nb >= 0 && nb <= p.max_blocks;
-    if (j == 0) {
-        p.item_seq[item] = item_ok ? s0 : 0;
-        p.item_ctx[item] = item_ok ? nb * kBlockSize : 0;
+    const int ni = p.num_items, W = p.width, tid = threadIdx.x;
+    for (int i = tid; i < p.num_counters; i += kSetupThreads) p.counters[i] = 0;
+    for (int s = tid; s < p.num_seqs; s += kSetupThreads) {
+        const int e = ni + s;
+        p.list_ctx[e] = p.context_lens[s];
+        p.list_seq[e] = s;
+        p.list_start[e] = 0;
+        p.list_rows[size_t(e) * W] = s;
+        for (int j = 1; j < W; ++j) p.list_rows[size_t(e) * W + j] = -1;
     }
-    int row = -1;
-    if (s >= 0) {
-        bool ok = item_ok && s < p.num_seqs && nb > 0 && p.context_lens[s] >= nb * kBlockSize;
-        for (int b = 0; ok && b < nb; ++b)
-            ok = p.block_tables[size_t(s) * p.max_blocks + b] == p.block_tables[size_t(s0) * p.max_blocks + b];
-        if (ok) ok = atomicCAS(&p.seq_start[s], 0, nb * kBlockSize) == 0;   // one item per sequence
-        if (ok) row = s;
-        else if (nb != 0 || !item_ok) flag_error(p.err, PKV_DEVERR_CASCADE);
+    for (int i = tid; i < ni; i += kSetupThreads) {
+        const int s0 = p.members[size_t(i) * W], nb = p.item_blocks[i];
+        const bool ok = s0 >= 0 && s0 < p.num_seqs && nb >= 0 && nb <= p.max_blocks;
+        p.list_ctx[i] = ok ? nb * kBlockSize : 0;
+        p.list_seq[i] = ok ? s0 : 0;
+        p.list_start[i] = 0;
     }
-    p.item_rows[i] = row;
+    __syncthreads();
+    const int warp = tid >> 5, lane = tid & 31;
+    for (int k = warp; k < ni * W; k += kSetupThreads / 32) {
+        const int item = k / W;
+        const int s = p.members[k], s0 = p.members[size_t(item) * W], nb = p.item_blocks[item];
+        bool ok = s0 >= 0 && s0 < p.num_seqs && nb > 0 && nb <= p.max_blocks && s >= 0 && s < p.num_seqs &&
+                  p.context_lens[s] >= nb * kBlockSize;
+        if (ok) {
+            const int32_t* a = p.block_tables + size_t(s) * p.max_blocks;
+            const int32_t* b = p.block_tables + size_t(s0) * p.max_blocks;
+            bool same = true;
+            for (int x = lane; x < nb; x += 32) same &= (a[x] == b[x]);
+            ok = __all_sync(0xffffffffu, same);
+        }
+        int row = -1;
+        if (lane == 0) {
+            // one item per sequence: the first to claim it
+            if (ok && atomicCAS(&p.list_start[ni + s], 0, nb * kBlockSize) == 0) row = s;
+            else if (s >= 0 && !(nb == 0 && s0 >= 0 && s0 < p.num_seqs)) flag_error(p.err, PKV_DEVERR_CASCADE);
+            p.list_rows[k] = row;
+        }
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_cascade_setup(const CascadeParams& p, cudaStream_t stream) {
-    const int n = p.num_items * p.width;
-    return launch_kernel(cascade_setup_kernel, dim3((n + kThreads - 1) / kThreads), dim3(kThreads), 0, stream, p);
+    return launch_kernel(cascade_setup_kernel, dim3(1), dim3(kSetupThreads), 0, stream, p);
 }
 
 }  // namespace pkv

@@ -91,7 +91,7 @@ def lib():
         L.pkv_cascade_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32, _I32, _I32]
         L.pkv_paged_attention_cascade.restype = st
         L.pkv_paged_attention_cascade.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
-                                                  _P, _P, _I32, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+                                                  _P, _P, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
         L.pkv_cascade_plan.restype = st
         L.pkv_cascade_plan.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.pkv_gather_kv_cache.restype = st
@@ -321,22 +321,22 @@ def pkv_cascade_plan(block_tables: torch.Tensor, context_lens: torch.Tensor, ite
     return members[:k].clone(), blocks[:k].clone()
 
 
-def pkv_cascade_workspace_bytes(num_seqs: int, num_heads: int, head_dim: int, max_blocks_per_seq: int,
-                                partition_size: int, num_items: int) -> int:
-    return int(lib().pkv_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_blocks_per_seq,
-                                                 partition_size, num_items))
+def pkv_cascade_workspace_bytes(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                                num_items: int, item_width: int) -> int:
+    return int(lib().pkv_cascade_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, num_items,
+                                                 item_width))
 
 
-def cascade_workspace(num_seqs: int, num_heads: int, head_dim: int, max_blocks_per_seq: int, partition_size: int,
-                      num_items: int, device="cuda") -> torch.Tensor:
-    n = pkv_cascade_workspace_bytes(num_seqs, num_heads, head_dim, max_blocks_per_seq, partition_size, num_items)
+def cascade_workspace(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, num_items: int,
+                      item_width: int, device="cuda") -> torch.Tensor:
+    """Caller-side scratch for pkv_paged_attention_cascade (needs no clearing)."""
+    n = pkv_cascade_workspace_bytes(num_seqs, num_heads, num_kv_heads, head_dim, num_items, item_width)
     return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
 
 
 def pkv_paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, scale: float, cache: Cache, seqs: Seqs,
-                                members: torch.Tensor, item_blocks: torch.Tensor, partition_size: int,
-                                workspace: torch.Tensor, err_flags: Optional[torch.Tensor] = None,
-                                stream=None) -> torch.Tensor:
+                                members: torch.Tensor, item_blocks: torch.Tensor, workspace: torch.Tensor,
+                                err_flags: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """Decode attention with each item's shared prefix read once for all its
     members (device int32 members [num_items, width], item_blocks [num_items])."""
     if members.dtype != torch.int32 or item_blocks.dtype != torch.int32:
@@ -349,7 +349,7 @@ def pkv_paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, scale: float
                                              float(scale), ctypes.byref(c), ctypes.byref(s),
                                              _ptr(members) if num_items else None,
                                              _ptr(item_blocks) if num_items else None, num_items,
-                                             max(width, 1), int(partition_size), _ptr(workspace),
+                                             max(width, 1), _ptr(workspace),
                                              int(workspace.numel() * workspace.element_size()),
                                              _err_ptr(err_flags), _stream(stream)))
     return out

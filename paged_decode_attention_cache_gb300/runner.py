@@ -27,9 +27,8 @@ class DecodeStep:
         (fixed partitions of partition_size tokens + LSE reduce) or "balanced"
         (equal block ranges per SM, combine fused) or "fused" (balanced, with the
         step's cache write in the same launch) or "cascade" (shared whole-page
-        prefixes read once per group, partitions of partition_size tokens, 512
-        by default); by default split when the workload names a partition size,
-        else single."""
+        prefixes read once per group, balanced); by default split when the
+        workload names a partition size, else single."""
         self.w = w
         self.device = device
         dev = torch.device(device)
@@ -38,9 +37,7 @@ class DecodeStep:
             schedule = "split" if self.partition_size > 0 else "single"
         if schedule not in ("single", "split", "balanced", "fused", "cascade"):
             raise ValueError(schedule)
-        if schedule == "cascade":
-            self.partition_size = self.partition_size or 512
-        elif schedule != "split":
+        if schedule != "split":
             self.partition_size = 0
         self.schedule = schedule
         self.seqs = ops.Seqs(w.block_tables.to(dev).contiguous(), w.context_lens.to(dev).contiguous(), w.q_len,
@@ -81,8 +78,8 @@ class DecodeStep:
                                                    min_shared_blocks=cascade_min_shared_blocks)
             self.members = members.to(dev).contiguous()
             self.item_blocks = blocks.to(dev).contiguous()
-            self.cascade_ws = ops.cascade_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_blocks,
-                                                    self.partition_size, int(members.shape[0]), device=dev)
+            self.cascade_ws = ops.cascade_workspace(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                    int(members.shape[0]), width, device=dev)
 
     @property
     def split(self) -> bool:
@@ -107,8 +104,7 @@ class DecodeStep:
                                              self.err, stream)
         elif self.schedule == "cascade":
             ops.pkv_paged_attention_cascade(self.out, self.q, self.w.scale, self.cache, self.seqs, self.members,
-                                            self.item_blocks, self.partition_size, self.cascade_ws, self.err,
-                                            stream)
+                                            self.item_blocks, self.cascade_ws, self.err, stream)
         elif self.schedule == "fused":
             ops.pkv_decode_step_balanced(self.out, self.q, self.w.scale, self.cache, self.seqs, self.k_new,
                                          self.v_new, self.slot_new, self.bal_ws, self.err, stream)
@@ -130,8 +126,7 @@ class DecodeStep:
         """Kernels of this library one step launches (clearing memsets not counted)."""
         wr = int(self.k_new.shape[0] > 0 and self.schedule != "fused")
         if self.schedule == "cascade":
-            items = int(self.members.shape[0]) > 0
-            return wr + 2 + 2 * int(items)   # [set-up], suffix, [prefix], reduce
+            return wr + 3   # set-up, attention, reduce
         return wr + 1 + int(self.split)
 
     def gather(self, stream=None):

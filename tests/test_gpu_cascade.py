@@ -28,9 +28,8 @@ def _built():
     torch.cuda.set_device(0)
 
 
-def run_cascade(w, part, min_shared=1):
-    st = DecodeStep(w, "cuda", partition_size=part, out_dtype=torch.float32, schedule="cascade",
-                    cascade_min_shared_blocks=min_shared)
+def run_cascade(w, min_shared=1):
+    st = DecodeStep(w, "cuda", out_dtype=torch.float32, schedule="cascade", cascade_min_shared_blocks=min_shared)
     out = st.step()
     torch.cuda.synchronize()
     assert st.error_flags() == 0, f"device error flags {st.error_flags():#x}"
@@ -41,24 +40,25 @@ GROUPS = [[0, 1, 2, 3, 4], [5, 6], [8, 9, 10]]
 CTX = [81, 100, 300, 97, 81, 90, 200, 50, 81, 81, 700, 17]
 
 
-@pytest.mark.parametrize("part", [16, 48, 512])
+@pytest.mark.parametrize("shared", [1, 5, 8])
 @pytest.mark.parametrize("dt,H,Hkv,D", [("bf16", 32, 8, 128), ("f16", 4, 4, 64), ("bf16", 16, 2, 128),
                                         ("f16", 8, 1, 64)])
-def test_cascade_decode(part, dt, H, Hkv, D):
-    w = W.build(name="t", seed=700 + H + D + part, context_lens=CTX, num_heads=H, num_kv_heads=Hkv, head_dim=D,
-                cache=dt, prefix_groups=GROUPS, shared_blocks=5)
+def test_cascade_decode(shared, dt, H, Hkv, D):
+    ctx = [c + 16 * (shared - 5) if c > 80 else c for c in CTX]
+    w = W.build(name="t", seed=700 + H + D + shared, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
+                cache=dt, prefix_groups=GROUPS, shared_blocks=shared)
     ref = oracle_attention(w, threads=8)
-    st, got = run_cascade(w, part)
+    st, got = run_cascade(w)
     assert st.members.shape[0] >= 3   # every group (or its cut) became an item
     check_attention(got, ref, False)
 
 
-@pytest.mark.parametrize("part", [32, 512])
-def test_cascade_k8v4(part):
-    w = W.build(name="t", seed=710 + part, context_lens=CTX, num_heads=8, num_kv_heads=2, head_dim=128,
+@pytest.mark.parametrize("H,Hkv", [(8, 2), (32, 8)])
+def test_cascade_k8v4(H, Hkv):
+    w = W.build(name="t", seed=710 + H, context_lens=CTX, num_heads=H, num_kv_heads=Hkv, head_dim=128,
                 cache="k8v4", prefix_groups=GROUPS, shared_blocks=5)
     ref = oracle_attention(w, threads=8)
-    _, got = run_cascade(w, part)
+    _, got = run_cascade(w)
     assert np.isfinite(got).all()
     assert np.abs(got - ref).max() <= K8V4_ABS
 
@@ -70,7 +70,7 @@ def test_cascade_wide_group_and_empty_suffix():
     w = W.build(name="t", seed=720, context_lens=ctx, num_heads=4, num_kv_heads=4, head_dim=64, cache="f16",
                 prefix_groups=[list(range(19))], shared_blocks=4, new_tokens="none")
     ref = oracle_attention(w, threads=8)
-    st, got = run_cascade(w, 64)
+    st, got = run_cascade(w)
     sizes = (st.members >= 0).sum(1).tolist()
     assert sorted(sizes) == [9, 10]
     check_attention(got, ref, False)
@@ -80,7 +80,7 @@ def test_cascade_no_items_is_plain_attention():
     w = W.build(name="t", seed=730, context_lens=[1, 16, 17, 300], num_heads=8, num_kv_heads=2, head_dim=128,
                 cache="bf16")
     ref = oracle_attention(w, threads=8)
-    st, got = run_cascade(w, 32)
+    st, got = run_cascade(w)
     assert st.members.shape[0] == 0
     check_attention(got, ref, False)
 
@@ -101,8 +101,8 @@ def test_cascade_bad_grouping_flags_and_stays_exact():
     members = torch.tensor([[0, 1, 4, 3], [2, 0, 99, -1]], dtype=torch.int32, device=dev)
     blocks = torch.tensor([5, 5], dtype=torch.int32, device=dev)
     out = torch.empty_like(st.out)
-    ws = ops.cascade_workspace(w.num_seqs, w.num_heads, w.head_dim, w.max_blocks, 32, 2, device=dev)
-    ops.pkv_paged_attention_cascade(out, st.q, w.scale, st.cache, st.seqs, members, blocks, 32, ws, st.err)
+    ws = ops.cascade_workspace(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, 2, 4, device=dev)
+    ops.pkv_paged_attention_cascade(out, st.q, w.scale, st.cache, st.seqs, members, blocks, ws, st.err)
     torch.cuda.synchronize()
     assert st.error_flags() & PKV_DEVERR_CASCADE
     check_attention(out.double().cpu().numpy(), ref, False)
@@ -113,8 +113,7 @@ def test_cascade_half_out(out_dt):
     w = W.build(name="t", seed=750, context_lens=CTX, num_heads=32, num_kv_heads=8, head_dim=128, cache="bf16",
                 prefix_groups=GROUPS, shared_blocks=5)
     ref = oracle_attention(w, threads=8)
-    st = DecodeStep(w, "cuda", partition_size=64, out_dtype=out_dt, schedule="cascade",
-                    cascade_min_shared_blocks=1)
+    st = DecodeStep(w, "cuda", out_dtype=out_dt, schedule="cascade", cascade_min_shared_blocks=1)
     got = st.step()
     torch.cuda.synchronize()
     assert st.error_flags() == 0
@@ -127,6 +126,6 @@ def test_cascade_serving_shape_sampled():
     w = W.cascade_b32_p2048(device="cpu")
     rows = list(range(0, w.num_rows, 5))
     ref = oracle_attention(w, rows=rows, threads=16)
-    st, got = run_cascade(w, 512, min_shared=8)
+    st, got = run_cascade(w, min_shared=8)
     assert st.members.shape[0] == 8
     check_attention(got[rows], ref[rows], False)
