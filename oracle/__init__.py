@@ -102,7 +102,7 @@ def _declare(L):
     L.pkvo_quantize_kv.argtypes = [_P, _P, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I]
     L.pkvo_paged_attention.restype = _I
     L.pkvo_paged_attention.argtypes = ([_P, _P, _P, _P, _I, _I, _P, _I, _I, _D, _I] + [_P] * 5 +
-                                       [_I] * 5 + [_P, _P, _I, _I, _I, _P, _I, _I, _I])
+                                       [_I] * 5 + [_P, _P, _I, _I, _I, _P, _I, _I, _I, _P, _P, _I])
     L.pkvo_gather_kv_cache_dequant.restype = _I
     L.pkvo_gather_kv_cache_dequant.argtypes = [_P, _P, _I, _P] + [_P] * 5 + [_P, _P] + [_I] * 7
     L.pkvo_lse_reduce.restype = None
@@ -243,7 +243,8 @@ def paged_attention(q_bits: np.ndarray, q_dtype: int, scale: float, cache_kind: 
                     k_cache, v_cache, block_tables, context_lens, q_len: int = 1,
                     k_scale=None, v_scale=None, v_zero=None, v_group: int = 32,
                     partition_size: int = 0, max_partitions: int = 0, rows=None,
-                    threads: int = 1, want_out: bool = True, window: int = 0):
+                    threads: int = 1, want_out: bool = True, window: int = 0,
+                    page_lists=None, page_counts=None):
     """fp64 paged attention.
 
     q_bits: [R, H, D] raw bits (uint16) for F16/BF16 (or float32/float64 with
@@ -252,7 +253,9 @@ def paged_attention(q_bits: np.ndarray, q_dtype: int, scale: float, cache_kind: 
     not computed when ``rows`` is given) and, if partition_size > 0,
     (part_o, part_m, part_l).  window > 0 keeps the last ``window`` stored
     tokens of each sequence visible (partitions wholly before them come back
-    empty: o = 0, m = -inf, l = 0).
+    empty: o = 0, m = -inf, l = 0).  page_lists [B, max_pages] / page_counts [B]
+    (int32): sparse page-indirection decode, each row attending only the tokens
+    of its sequence's listed logical pages (no partitions).
     """
     q = np.ascontiguousarray(q_bits)
     R, H, D = q.shape
@@ -270,13 +273,19 @@ def paged_attention(q_bits: np.ndarray, q_dtype: int, scale: float, cache_kind: 
         part = (np.zeros((R, H, max_partitions, D)), np.zeros((R, H, max_partitions)),
                 np.zeros((R, H, max_partitions)))
     rl = None if rows is None else _c(np.asarray(rows, np.int32), np.int32)
+    pl = pc = None
+    if page_lists is not None:
+        pl = _c(page_lists, np.int32)
+        pc = _c(page_counts, np.int32)
+        assert pl.ndim == 2 and pl.shape[0] == bt.shape[0] and pc.shape == (bt.shape[0],)
     rc = lib().pkvo_paged_attention(
         _ptr(out), _ptr(part[0]) if part else None, _ptr(part[1]) if part else None,
         _ptr(part[2]) if part else None, partition_size, max_partitions, _ptr(q), q_dtype, H,
         float(scale), cache_kind, _ptr(np.ascontiguousarray(k_cache)),
         _ptr(np.ascontiguousarray(v_cache)), _ptr(k_scale), _ptr(v_scale), _ptr(v_zero), NB, bs,
         Hkv, D, v_group, _ptr(bt), _ptr(cl), bt.shape[0], bt.shape[1], q_len, _ptr(rl),
-        0 if rl is None else rl.size, threads, int(window))
+        0 if rl is None else rl.size, threads, int(window), _ptr(pl), _ptr(pc),
+        0 if pl is None else pl.shape[1])
     if rc:
         raise ValueError(f"oracle attention failed ({rc})")
     if part is not None:

@@ -302,6 +302,9 @@ typedef struct {
     const int32_t *block_tables, *context_lens;
     int num_seqs, max_blocks, q_len;
     int window;   /* sliding window in tokens, 0 = none */
+    /* sparse page indirection (optional): pages of each sequence to attend */
+    const int32_t *page_lists, *page_counts;
+    int max_pages;
     /* work */
     const int32_t *row_list;
     int n_rows, n_threads, thread_id;
@@ -387,6 +390,59 @@ static int attend_range(const attn_job *J, int s, int kvh, const double *qd, int
     return 0;
 }
 
+/* The same attention over an explicit list of logical tokens tok[0..n) (in
+ * increasing order), for sparse page-indirection decode. */
+static int attend_list(const attn_job *J, int s, int kvh, const double *qd, const int *tok, int n,
+                       double *o, double *m_out, double *l_out, double *x, double *row)
+{
+    int D = J->head_dim;
+    for (int d = 0; d < D; d++) o[d] = 0.0;
+    if (n <= 0) { *m_out = -INFINITY; *l_out = 0.0; return 0; }
+    double m = -INFINITY;
+    for (int i = 0; i < n; i++) {
+        if (load_k_row(J, s, tok[i], kvh, row)) return -1;
+        double dot = 0.0;
+        for (int d = 0; d < D; d++) dot += qd[d] * row[d];
+        x[i] = J->scale * dot;
+        if (x[i] > m) m = x[i];
+    }
+    double l = 0.0;
+    for (int i = 0; i < n; i++) {
+        double w = exp(x[i] - m);
+        l += w;
+        if (load_v_row(J, s, tok[i], kvh, row)) return -1;
+        for (int d = 0; d < D; d++) o[d] += w * row[d];
+    }
+    for (int d = 0; d < D; d++) o[d] /= l;
+    *m_out = m;
+    *l_out = l;
+    return 0;
+}
+
+/* Tokens a sparse page list makes visible in [lo, vis) [MLXCEL §"Paged Decode
+ * Storage and Kernels": sparse page-indirection decode].  Reading: the list
+ * names logical pages (16-token blocks) of the sequence; page p contributes its
+ * tokens p*16 .. p*16+15 that lie in [lo, vis).  Entries are taken in order;
+ * one that is outside [0, ceil(ctx / 16)) or not above the last page taken is
+ * skipped.  Returns the number of tokens written to tok. */
+static int sparse_tokens(const attn_job *J, int s, int ctx, int lo, int vis, int *tok)
+{
+    int bs = J->block_size, n = 0, last = -1;
+    int cnt = J->page_counts[s];
+    if (cnt > J->max_pages) cnt = J->max_pages;
+    int npages = (ctx + bs - 1) / bs;
+    for (int i = 0; i < cnt; i++) {
+        int p = J->page_lists[(size_t)s * J->max_pages + i];
+        if (p < 0 || p >= npages || p <= last) continue;
+        last = p;
+        for (int o = 0; o < bs; o++) {
+            int t = p * bs + o;
+            if (t >= lo && t < vis) tok[n++] = t;
+        }
+    }
+    return n;
+}
+
 static void *attn_worker(void *arg)
 {
     attn_job *J = (attn_job *)arg;
@@ -396,6 +452,7 @@ static void *attn_worker(void *arg)
     double *qd = (double *)malloc(sizeof(double) * (size_t)D);
     double *row = (double *)malloc(sizeof(double) * (size_t)D);
     double *x = (double *)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
+    int *tok = J->page_lists ? (int *)malloc(sizeof(int) * (size_t)(cap > 0 ? cap : 1)) : NULL;
     double m, l;
     for (long task = J->thread_id; task < (long)R * H; task += J->n_threads) {
         int r = J->row_list ? J->row_list[task / H] : (int)(task / H);
@@ -421,7 +478,10 @@ static void *attn_worker(void *arg)
         int kvh = h / g;
         size_t qoff = ((size_t)r * H + h) * D;
         for (int d = 0; d < D; d++) qd[d] = load_elem(J->q, J->q_dtype, qoff + d);
-        if (J->out) {
+        if (J->out && J->page_lists) {
+            int n = sparse_tokens(J, s, ctx, lo, vis, tok);
+            if (attend_list(J, s, kvh, qd, tok, n, J->out + qoff, &m, &l, x, row)) { J->error = -1; break; }
+        } else if (J->out) {
             if (attend_range(J, s, kvh, qd, lo, vis, J->out + qoff, &m, &l, x, row)) { J->error = -1; break; }
         }
         if (J->part_o) {
@@ -441,6 +501,7 @@ static void *attn_worker(void *arg)
     free(qd);
     free(row);
     free(x);
+    free(tok);
     return NULL;
 }
 
@@ -451,8 +512,10 @@ static void *attn_worker(void *arg)
  * [R, H, max_partitions] (m_p in the units of scale * q.k, natural log base).
  * row_list (optional) restricts the work to the listed rows; the other rows of
  * out are left untouched.  window > 0 keeps only the last `window` stored tokens
- * of each sequence visible.  Returns 0, or a negative code on an out-of-range
- * block id (-1) or a context longer than its table (-2). */
+ * of each sequence visible.  page_lists [num_seqs, max_pages] / page_counts
+ * [num_seqs] (optional, out only): each row attends only the tokens of its
+ * sequence's listed pages (sparse_tokens).  Returns 0, or a negative code on an
+ * out-of-range block id (-1) or a context longer than its table (-2). */
 int pkvo_paged_attention(double *out, double *part_o, double *part_m, double *part_l,
                          int partition_size, int max_partitions, const void *q, int q_dtype,
                          int num_heads, double scale, int cache_kind, const void *k_cache,
@@ -460,16 +523,19 @@ int pkvo_paged_attention(double *out, double *part_o, double *part_m, double *pa
                          const void *v_zero, int num_blocks, int block_size, int num_kv_heads,
                          int head_dim, int v_group, const int32_t *block_tables,
                          const int32_t *context_lens, int num_seqs, int max_blocks, int q_len,
-                         const int32_t *row_list, int n_rows, int n_threads, int window)
+                         const int32_t *row_list, int n_rows, int n_threads, int window,
+                         const int32_t *page_lists, const int32_t *page_counts, int max_pages)
 {
     if (window < 0) return -3;
     if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return -3;
     if (part_o && partition_size <= 0) return -3;
+    if (page_lists && (part_o || !page_counts || max_pages < 0)) return -3;
     if (n_threads < 1) n_threads = 1;
     attn_job base = {out, part_o, part_m, part_l, partition_size, max_partitions, q, q_dtype,
                      num_heads, scale, cache_kind, k_cache, v_cache, k_scale, v_scale, v_zero,
                      num_blocks, block_size, num_kv_heads, head_dim, v_group, block_tables,
-                     context_lens, num_seqs, max_blocks, q_len, window, row_list, n_rows, n_threads, 0, 0};
+                     context_lens, num_seqs, max_blocks, q_len, window, page_lists, page_counts,
+                     max_pages, row_list, n_rows, n_threads, 0, 0};
     attn_job *jobs = (attn_job *)malloc(sizeof(attn_job) * (size_t)n_threads);
     pthread_t *th = (pthread_t *)malloc(sizeof(pthread_t) * (size_t)n_threads);
     for (int i = 0; i < n_threads; i++) {

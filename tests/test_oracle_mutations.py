@@ -9,6 +9,7 @@ import pytest
 import oracle
 from tests import test_oracle_attention as TA
 from tests import test_oracle_cache as TC
+from tests import test_oracle_sparse as TS
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "pkv_oracle.c")
 
@@ -43,6 +44,10 @@ MUTANTS = [
     ("window per draft row", "if (J->window > 0 && ctx > J->window) lo = ctx - J->window;",
      "if (J->window > 0 && vis > J->window) lo = vis - J->window;",
      lambda: TA.test_window_matches_sdpa_over_the_last_tokens(*TA.WINDOW_CASES[2])),
+    ("sparse page token offset", "int t = p * bs + o;", "int t = p * bs + o + 1;",
+     lambda: TS.test_sparse_matches_sdpa_over_listed_pages(*TS.CASES[0])),
+    ("sparse repeated page kept", "if (p < 0 || p >= npages || p <= last) continue;",
+     "if (p < 0 || p >= npages || p < last) continue;", TS.test_bad_entries_are_skipped),
 ]
 
 
