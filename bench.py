@@ -43,6 +43,7 @@ WORKLOADS = {
     "verify_batch256": 5,
     "sliding_window_b8_w4096": "sliding_window_b8_w4096",
     "cascade_b32_p2048": "cascade_b32_p2048",
+    "sparse_b4_32k": "sparse_b4_32k",
 }
 DEFAULT_WORKLOAD = "llama3_8b_batch8"
 # schedule of the attention call per workload: the 32K workload is defined with
@@ -52,10 +53,11 @@ DEFAULT_WORKLOAD = "llama3_8b_batch8"
 # one is a single pass
 DEFAULT_SCHEDULE = {"tiny_f16": "single", "llama3_8b_batch8": "fused", "long_context_32k": "split",
                     "k8v4_batch32": "fused", "verify_batch256": "balanced",
-                    "sliding_window_b8_w4096": "fused", "cascade_b32_p2048": "cascade"}
+                    "sliding_window_b8_w4096": "fused", "cascade_b32_p2048": "cascade",
+                    "sparse_b4_32k": "sparse"}
 KERNEL_NAME = {"single": "pkv_paged_attention", "split": "pkv_paged_attention_split",
                "balanced": "pkv_paged_attention_balanced", "fused": "pkv_decode_step_balanced",
-               "cascade": "pkv_paged_attention_cascade"}
+               "cascade": "pkv_paged_attention_cascade", "sparse": "pkv_paged_attention_sparse"}
 
 
 def parse():
@@ -65,7 +67,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--partition", type=int, default=None, help="split-KV partition size (with --schedule split)")
-    ap.add_argument("--schedule", default=None, choices=["single", "split", "balanced", "fused", "cascade"],
+    ap.add_argument("--schedule", default=None,
+                    choices=["single", "split", "balanced", "fused", "cascade", "sparse"],
                     help="attention schedule (default: per workload)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -112,12 +115,16 @@ def make_workload(name, device, seed_offset=0, partition=None):
     return w
 
 
-def step_bytes(w, cascade_plan=None):
+def step_bytes(w, cascade_plan=None, sparse=False):
     """(attention bytes, write bytes) of one step; cascade_plan = (members,
-    item_blocks) counts each item's shared prefix once."""
+    item_blocks) counts each item's shared prefix once; sparse counts only the
+    listed pages."""
     from paged_decode_attention_cache_gb300 import bytes_model as BM
     ctx = [int(c) for c in w.context_lens.cpu()]
-    if cascade_plan is not None:
+    if sparse:
+        attn = BM.sparse_attention_bytes(ctx, w.page_lists.cpu().tolist(), w.page_counts.cpu().tolist(),
+                                         w.num_heads, w.num_kv_heads, w.head_dim, w.cache)
+    elif cascade_plan is not None:
         members, blocks = (x.cpu().tolist() for x in cascade_plan)
         attn = BM.cascade_attention_bytes(ctx, members, blocks, w.num_heads, w.num_kv_heads, w.head_dim, w.cache)
     else:
@@ -199,7 +206,7 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(w, attn_bytes, budget_s, split=False):
+def cpu_baseline(w, attn_bytes, budget_s, split=False, sparse=False):
     """The oracle as it stands, on this host's cores, over whole steps of the
     same workload until the time budget is spent (at least one step)."""
     import numpy as np  # noqa: F401
@@ -210,7 +217,9 @@ def cpu_baseline(w, attn_bytes, budget_s, split=False):
     split = split and w.partition_size > 0
     n, t0 = 0, time.perf_counter()
     while True:
-        if split:   # phase 1 partials, then the LSE reduce, as the GPU step does
+        if sparse:   # only the listed pages
+            oracle_attention(w, cs, threads=threads, sparse=True)
+        elif split:   # phase 1 partials, then the LSE reduce, as the GPU step does
             _, part = oracle_attention(w, cs, threads=threads, partition_size=w.partition_size,
                                        max_partitions=w.max_partitions, want_out=False)
             oracle.lse_reduce(*part)
@@ -231,9 +240,16 @@ def run_reference(args):
     if rank != 0:
         return 0
     w = make_workload(args.workload, "cpu", 0, args.partition)
-    attn_b, wr_b = step_bytes(w)
     schedule = args.schedule or DEFAULT_SCHEDULE[args.workload]
-    cb = cpu_baseline(w, attn_b + wr_b, max(1.0, min(args.cpu_seconds, 20.0)), split=(schedule == "split"))
+    plan = None
+    if schedule == "cascade":   # bytes as the GPU arm counts them (the oracle itself is plain attention)
+        from paged_decode_attention_cache_gb300 import build as pkv_build, ops
+        from paged_decode_attention_cache_gb300.runner import cascade_plan_for
+        pkv_build.build()
+        plan = cascade_plan_for(w)
+    attn_b, wr_b = step_bytes(w, plan, sparse=(schedule == "sparse"))
+    cb = cpu_baseline(w, attn_b + wr_b, max(1.0, min(args.cpu_seconds, 20.0)), split=(schedule == "split"),
+                      sparse=(schedule == "sparse"))
     line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": cb["seconds_per_step"] * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -271,7 +287,7 @@ def main():
         w.partition_size = 512
     first = DecodeStep(w, dev, schedule=schedule)
     plan = (first.members, first.item_blocks) if schedule == "cascade" else None
-    attn_b, wr_b = step_bytes(w, plan)
+    attn_b, wr_b = step_bytes(w, plan, sparse=(schedule == "sparse"))
     total_b = attn_b + wr_b
     l2 = getattr(torch.cuda.get_device_properties(local), "L2_cache_size", 0) or L2_BYTES_FALLBACK
     reps = max(2, math.ceil(3 * l2 / max(1, total_b)))
@@ -357,6 +373,8 @@ def main():
         src = [st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens]
         if schedule == "cascade":
             src += [st.members, st.item_blocks]
+        if schedule == "sparse":
+            src += [st.page_lists, st.page_counts]
         offs, total = [], 0
         for x in src:
             offs.append(total)
@@ -371,6 +389,8 @@ def main():
         st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens = views[:6]
         if schedule == "cascade":
             st.members, st.item_blocks = views[6:]
+        if schedule == "sparse":
+            st.page_lists, st.page_counts = views[6:]
         host_out = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
         h2d = total
         d2h = host_out.numel() * host_out.element_size()
@@ -408,7 +428,7 @@ def main():
     cb = None
     if rank == 0 and not (args.no_cpu_baseline or args.quick):
         wc = make_workload(args.workload, "cpu", 0, args.partition)
-        cb = cpu_baseline(wc, total_b, args.cpu_seconds, split=(schedule == "split"))
+        cb = cpu_baseline(wc, total_b, args.cpu_seconds, split=(schedule == "split"), sparse=(schedule == "sparse"))
         cb.pop("seconds_per_step", None)
 
     if ws > 1:
@@ -426,6 +446,8 @@ def main():
                    "sum_context": int(w.context_lens.sum()),
                    **({"cascade_items": int(first.members.shape[0]),
                        "plain_attention_bytes": step_bytes(w)[0]} if schedule == "cascade" else {}),
+                   **({"pages_listed": int(w.page_counts.sum()),
+                       "dense_attention_bytes": step_bytes(w)[0]} if schedule == "sparse" else {}),
                    "bytes_per_step": total_b, "parallelism": f"replicas x{ws}",
                    "l2": f"{reps} rotating input replicas, {reps * total_b / 2**20:.0f} MiB touched per cycle "
                          f"vs {l2 / 2**20:.0f} MiB L2"},

@@ -62,6 +62,7 @@ typedef enum pkv_status {
 #define PKV_DEVERR_CAPACITY 0x4u   /* a context longer than its table or partitions */
 #define PKV_DEVERR_TIMEOUT 0x8u    /* a bounded pipeline wait gave up */
 #define PKV_DEVERR_CASCADE 0x10u   /* a cascade member could not join its item (attended whole) */
+#define PKV_DEVERR_PAGE_LIST 0x20u /* a sparse page-list entry was skipped (out of range or out of order) */
 
 typedef enum pkv_dtype { PKV_F16 = 0, PKV_BF16 = 1, PKV_F32 = 2 } pkv_dtype;
 
@@ -314,6 +315,40 @@ pkv_status pkv_paged_attention_cascade(void *out, pkv_dtype out_dtype, const voi
                                        const int32_t *members, const int32_t *item_blocks, int32_t num_items,
                                        int32_t item_width, void *workspace, size_t workspace_bytes,
                                        uint32_t *err_flags, pkv_stream_t stream);
+
+/*
+ * Sparse page-indirection decode [MLXCEL §"Paged Decode Storage and Kernels":
+ * sparse page-indirection decode, a KV-traffic deletion (METAL, "Long context
+ * turns decode into a cache-streaming benchmark")].  Each sequence attends only
+ * the stored tokens of the logical pages (16-token blocks) it lists; the other
+ * pages are never read.  q_len 1, no sliding window.
+ *   page_lists   int32 [num_seqs, max_pages] device: logical page indices in
+ *                increasing order; entries past page_counts[s] are ignored; an
+ *                entry outside [0, ceil(ctx / 16)) or not above the previous page
+ *                taken is skipped and flags PKV_DEVERR_PAGE_LIST.
+ *   page_counts  int32 [num_seqs] device.
+ *   workspace    pkv_sparse_workspace_bytes(...) bytes, 256-byte aligned; needs
+ *                no clearing.  Calls sharing a workspace must not overlap.
+ * Two launches on `stream`: a set-up kernel compacts the listed pages' block ids
+ * (one CTA per sequence), then the balanced attention streams the compacted
+ * tables (it plans once the set-up has finished).  A sequence that lists no
+ * page gets zeros.
+ */
+size_t pkv_sparse_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t max_pages);
+pkv_status pkv_paged_attention_sparse(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
+                                      int32_t num_heads, float scale, const pkv_cache *cache, const pkv_seqs *seqs,
+                                      const int32_t *page_lists, const int32_t *page_counts, int32_t max_pages,
+                                      void *workspace, size_t workspace_bytes, uint32_t *err_flags,
+                                      pkv_stream_t stream);
+
+/*
+ * Whether sparse page-indirection is worth using [MLXCEL §"Paged Decode Storage
+ * and Kernels": a minimum sparsity gates it]: 1 if the listed pages leave out at
+ * least min_sparsity of the pages of all sequences (HOST arrays: page_counts,
+ * context_lens [num_seqs]), else 0.  Counts are clamped to each context's pages.
+ */
+int32_t pkv_sparse_worthwhile(const int32_t *page_counts, const int32_t *context_lens, int32_t num_seqs,
+                              float min_sparsity);
 
 /*
  * Host-side grouping for pkv_paged_attention_cascade [MLXCEL §"Paged Decode

@@ -79,6 +79,31 @@ def cascade_attention_bytes(context_lens, members, item_blocks, num_heads: int, 
     return kv + qo + tables
 
 
+def sparse_attention_bytes(context_lens, page_lists, page_counts, num_heads: int, num_kv_heads: int,
+                           head_dim: int, cache: str, q_bytes: int = 2, out_bytes: int = 2,
+                           v_group: int = 32) -> int:
+    """Sparse page-indirection decode (q_len 1) [mlxcel manual "KV Cache",
+    §"Paged Decode Storage and Kernels"]: K + V rows of the listed pages' stored
+    tokens only, q in, out back, the list entries and the listed pages' block
+    ids (read once, written compacted, read again), lengths.  Lists as the
+    oracle reads them: in order, pages in range and above the last one taken."""
+    kb, vb = row_bytes(cache, head_dim, v_group)
+    tokens, pages, entries = 0, 0, 0
+    for c, lst, n in zip(context_lens, page_lists, page_counts):
+        c, n = int(c), int(n)
+        npages, last = -(-c // BLOCK_SIZE), -1
+        entries += n
+        for p in list(lst)[:n]:
+            p = int(p)
+            if 0 <= p < npages and p > last:
+                last = p
+                pages += 1
+                tokens += min(BLOCK_SIZE, c - p * BLOCK_SIZE)
+    kv = tokens * num_kv_heads * (kb + vb)
+    qo = len(context_lens) * num_heads * head_dim * (q_bytes + out_bytes)
+    return kv + qo + 4 * entries + 3 * 4 * pages + 3 * 4 * len(context_lens)
+
+
 def write_bytes(num_tokens: int, num_kv_heads: int, head_dim: int, cache: str, src_bytes: int = 2,
                 v_group: int = 32) -> int:
     """New K/V rows read from the source and written to their slots."""

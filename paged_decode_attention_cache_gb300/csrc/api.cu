@@ -524,6 +524,80 @@ pkv_status pkv_paged_attention_cascade(void* out, pkv_dtype out_dtype, const voi
     return cuda_result(pkv::launch_reduce(r, cs), "cascade reduce launch");
 }
 
+size_t pkv_sparse_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t max_pages) {
+    if (num_seqs < 0 || num_kv_heads < 1 || head_dim < 1 || max_pages < 0) return 0;
+    return align256(size_t(num_seqs) * size_t(max_pages) * 4) + align256(size_t(num_seqs) * 4) +
+           pkv::balanced_workspace_bytes(num_seqs, num_kv_heads, head_dim);
+}
+
+pkv_status pkv_paged_attention_sparse(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
+                                      int32_t num_heads, float scale, const pkv_cache* cache, const pkv_seqs* seqs,
+                                      const int32_t* page_lists, const int32_t* page_counts, int32_t max_pages,
+                                      void* workspace, size_t workspace_bytes, uint32_t* err_flags,
+                                      pkv_stream_t stream) {
+    pkv::AttnParams p;
+    int gqa = 0;
+    pkv_status st = attn_setup(&p, q, q_dtype, num_heads, scale, cache, seqs, err_flags, &gqa);
+    if (st != PKV_OK) return st;
+    if (seqs->q_len != 1) return fail(PKV_ERR_UNSUPPORTED, "sparse page-indirection decode is for q_len 1");
+    if (seqs->sliding_window != 0) return fail(PKV_ERR_UNSUPPORTED, "sparse page-indirection with a sliding window");
+    if (max_pages < 1) return fail(PKV_ERR_INVALID_ARG, "max_pages %d", max_pages);
+    if (!page_lists || !page_counts) return fail(PKV_ERR_INVALID_ARG, "page_lists / page_counts is NULL");
+    if (int64_t(seqs->num_seqs) * max_pages > INT32_MAX / 2) return fail(PKV_ERR_INVALID_ARG, "page lists too large");
+    if (seqs->num_seqs == 0) return ok();
+    const size_t need = pkv_sparse_workspace_bytes(seqs->num_seqs, cache->num_kv_heads, cache->head_dim, max_pages);
+    if (!workspace) return fail(PKV_ERR_INVALID_ARG, "workspace is NULL");
+    if (workspace_bytes < need)
+        return fail(PKV_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, need);
+    uint8_t* w = static_cast<uint8_t*>(workspace);
+    int32_t* table_c = reinterpret_cast<int32_t*>(w);
+    w += align256(size_t(seqs->num_seqs) * size_t(max_pages) * 4);
+    int32_t* ctx_c = reinterpret_cast<int32_t*>(w);
+    w += align256(size_t(seqs->num_seqs) * 4);
+    if ((st = balanced_setup(p, out, out_dtype, cache, seqs, w, need - size_t(w - static_cast<uint8_t*>(workspace)))) !=
+        PKV_OK)
+        return st;
+    pkv::SparseParams sp{};
+    sp.page_lists = page_lists;
+    sp.page_counts = page_counts;
+    sp.block_tables = seqs->block_tables;
+    sp.context_lens = seqs->context_lens;
+    sp.num_seqs = seqs->num_seqs;
+    sp.max_pages = max_pages;
+    sp.max_blocks = seqs->max_blocks_per_seq;
+    sp.table_out = table_c;
+    sp.ctx_out = ctx_c;
+    sp.counters = p.counters;
+    sp.num_counters = seqs->num_seqs * cache->num_kv_heads;
+    sp.err = err_flags;
+    cudaError_t e = pkv::launch_sparse_setup(sp, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_result(e, "sparse set-up launch");
+    // the balanced attention over the compacted tables
+    p.block_tables = table_c;
+    p.context_lens = ctx_c;
+    p.max_blocks = max_pages;
+    p.partition_blocks = max_pages;
+    p.wait_first = 1;
+    return attn_launch(p, cache, gqa, stream);
+}
+
+int32_t pkv_sparse_worthwhile(const int32_t* page_counts, const int32_t* context_lens, int32_t num_seqs,
+                              float min_sparsity) {
+    if (!page_counts || !context_lens || num_seqs <= 0) return 0;
+    long long listed = 0, total = 0;
+    for (int s = 0; s < num_seqs; ++s) {
+        const long long pages = context_lens[s] > 0 ? (context_lens[s] + 15) / 16 : 0;
+        long long c = page_counts[s];
+        c = c < 0 ? 0 : (c > pages ? pages : c);
+        listed += c;
+        total += pages;
+    }
+    if (total == 0) return 0;
+    // min_sparsity arrives as a float: compare with a relative slack of 1e-6
+    const double skipped = double(total - listed);
+    return skipped >= double(min_sparsity) * double(total) * (1.0 - 1e-6) ? 1 : 0;
+}
+
 pkv_status pkv_decode_step_balanced(void* out, pkv_dtype out_dtype, const void* q, pkv_dtype q_dtype,
                                     int32_t num_heads, float scale, const pkv_cache* cache, const pkv_seqs* seqs,
                                     const void* k_new, const void* v_new, pkv_dtype src_dtype,

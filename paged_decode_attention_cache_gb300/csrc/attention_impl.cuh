@@ -1287,7 +1287,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     // so CTAs c .. c+Hkv-1 stream the same blocks' head slices side by side and
     // every 2*Hkv*D-byte token row of a block is read from DRAM at one time.
     const int lane_kvh = blockIdx.x % Hkv, lane_idx = blockIdx.x / Hkv, nlanes = gridDim.x / Hkv;
-    if constexpr (CASC) grid_dep_wait();   // the plan reads what the previous kernel wrote
+    if (CASC || p.wait_first) grid_dep_wait();   // the plan reads what the previous kernel wrote
     Plan pl;
     if (p.mode == kModeSingle) {
         const long long total = (long long)p.num_seqs * Hkv;
@@ -1303,8 +1303,8 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         cta_plan<CASC>(p, lane_idx, nlanes, red, flag, pl);
     }
     const long long chunk = pl.chunk;
-    // Except in a cascade pass, everything above read only the launch's inputs
-    // (context lengths), which no kernel of this library writes; what follows
+    // Except in a cascade pass or with wait_first, everything above read only the
+    // launch's inputs (context lengths), which no kernel of this library writes; what follows
     // waits for the previous kernel of the stream before it reads the cache or
     // writes anything.
     if (tid == 0) grid_dep_launch();
@@ -1710,8 +1710,8 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
         if (lane_units < L) L = int(lane_units < 1 ? 1 : lane_units);
         grid = L * p.num_kv_heads;
     }
-    return launch_kernel(attention_kernel<Math, FUSED, CASC>, dim3(grid), dim3((Math::NCW + 1) * 32), size_t(smem), stream,
-                         km, vm, p);
+    return launch_kernel(attention_kernel<Math, FUSED, CASC>, dim3(grid), dim3((Math::NCW + 1) * 32), size_t(smem),
+                         stream, km, vm, p);
 }
 
 template <typename T, int D, bool FUSED>

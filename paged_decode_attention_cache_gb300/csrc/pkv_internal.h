@@ -84,6 +84,9 @@ struct AttnParams {
     const int32_t* seq_start;
     int32_t num_items;
     int32_t part_offset;
+    // 1: block_tables / context_lens come from the previous kernel (the sparse
+    // set-up), so the kernel waits for it before planning
+    int32_t wait_first;
     float* part_o;      // balanced workspace: [slots, 16, head_dim] unnormalised partial outputs
     float* part_ml;     // [slots, 16, 2] (max, sum) in base-2 units
     int32_t* counters;  // [num_seqs * num_kv_heads] pieces finished per (sequence, kv head)
@@ -156,6 +159,22 @@ struct CascadeParams {
     uint32_t* err;
 };
 cudaError_t launch_cascade_setup(const CascadeParams& p, cudaStream_t stream);
+
+// Sparse page-indirection set-up (one CTA per sequence): the listed pages'
+// block ids, compacted, and the compacted context (the tail page may be partial).
+struct SparseParams {
+    const int32_t* page_lists;    // [num_seqs, max_pages]
+    const int32_t* page_counts;   // [num_seqs]
+    const int32_t* block_tables;
+    const int32_t* context_lens;
+    int32_t num_seqs, max_pages, max_blocks;
+    int32_t* table_out;           // out [num_seqs, max_pages]
+    int32_t* ctx_out;             // out [num_seqs]
+    int32_t* counters;            // the balanced pass's piece counters, cleared here
+    int32_t num_counters;
+    uint32_t* err;
+};
+cudaError_t launch_sparse_setup(const SparseParams& p, cudaStream_t stream);
 
 struct CacheWriteParams {
     void* k_cache;

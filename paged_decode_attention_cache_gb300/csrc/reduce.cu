@@ -1,4 +1,6 @@
-// reduce.cu -- split-KV phase 2: log-sum-exp combination of partition partials.
+// reduce.cu -- split-KV phase 2: log-sum-exp combination of partition partials;
+// also the small set-up kernels that build the work lists of cascade and sparse
+// page-indirection attention.
 //
 // The pages name split-KV decode [mlxcel manual "KV Cache", §"Paged Decode
 // Storage and Kernels": decode splits; metalworking "The KV Cache": split-KV
@@ -193,7 +195,85 @@ __global__ void __launch_bounds__(kSetupThreads) cascade_setup_kernel(CascadePar
     }
 }
 
+// Sparse page-indirection set-up [mlxcel manual "KV Cache", §"Paged Decode
+// Storage and Kernels": sparse page-indirection decode], one CTA per sequence,
+// 1024 list entries per round.  Entries are taken in order; one outside the
+// context's pages or not above the last page taken is skipped (and flagged): an
+// in-range entry is kept iff it exceeds every earlier in-range entry (a prefix
+// max over the list).  The kept pages' block ids are written back to back, so
+// the attention streams a compacted sequence: page k holds compacted tokens
+// [16k, 16k + 16), and only the context's tail page can be partial, so the
+// compacted context is 16 (n - 1) + (ctx - 16 (pages - 1)) when the tail page
+// is kept and 16 n otherwise.
+constexpr int kSparseThreads = 1024;
+constexpr int kSparseWarps = kSparseThreads / 32;
+
+__global__ void __launch_bounds__(kSparseThreads) sparse_setup_kernel(SparseParams p) {
+    grid_dep_wait();
+    grid_dep_launch();
+    __shared__ int w_max[kSparseWarps], w_cnt[kSparseWarps];
+    __shared__ int any_bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, s = blockIdx.x;
+    for (int i = s * kSparseThreads + tid; i < p.num_counters; i += gridDim.x * kSparseThreads) p.counters[i] = 0;
+    if (tid == 0) any_bad = 0;
+    int ctx = p.context_lens[s];
+    if (ctx < 0) ctx = 0;
+    if (ctx > p.max_blocks * kBlockSize) {
+        ctx = p.max_blocks * kBlockSize;
+        if (tid == 0) flag_error(p.err, PKV_DEVERR_CAPACITY);
+    }
+    const int npages = (ctx + kBlockSize - 1) / kBlockSize;
+    int cnt = p.page_counts[s];
+    cnt = cnt < 0 ? 0 : (cnt > p.max_pages ? p.max_pages : cnt);
+    const int32_t* list = p.page_lists + size_t(s) * p.max_pages;
+    const int32_t* bt = p.block_tables + size_t(s) * p.max_blocks;
+    int32_t* out = p.table_out + size_t(s) * p.max_pages;
+    int last = -1, n = 0;   // the largest page taken so far, pages taken so far
+    for (int base = 0; base < cnt; base += kSparseThreads) {
+        const int i = base + tid;
+        const int pg = i < cnt ? list[i] : -1;
+        const bool in_range = i < cnt && pg >= 0 && pg < npages;
+        // inclusive prefix max of in-range pages within the warp
+        int incl = in_range ? pg : -1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl = max(incl, t);
+        }
+        if (lane == 31) w_max[warp] = incl;
+        __syncthreads();
+        int before = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) before = -1;
+        before = max(before, last);
+        for (int w2 = 0; w2 < warp; ++w2) before = max(before, w_max[w2]);
+        const bool keep = in_range && pg > before;
+        if (i < cnt && !keep) any_bad = 1;
+        const unsigned m = __ballot_sync(0xffffffffu, keep);
+        if (lane == 0) w_cnt[warp] = __popc(m);
+        __syncthreads();
+        int pos = n + __popc(m & ((1u << lane) - 1u));
+        for (int w2 = 0; w2 < warp; ++w2) pos += w_cnt[w2];
+        if (keep) out[pos] = bt[pg];
+        for (int w2 = 0; w2 < kSparseWarps; ++w2) {
+            n += w_cnt[w2];
+            last = max(last, w_max[w2]);
+        }
+        __syncthreads();   // w_max / w_cnt are rewritten by the next round
+    }
+    if (tid == 0) {
+        if (any_bad) flag_error(p.err, PKV_DEVERR_PAGE_LIST);
+        p.ctx_out[s] = n == 0 ? 0
+                              : (last == npages - 1 ? kBlockSize * (n - 1) + (ctx - kBlockSize * (npages - 1))
+                                                    : kBlockSize * n);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_sparse_setup(const SparseParams& p, cudaStream_t stream) {
+    if (p.num_seqs < 1) return cudaSuccess;
+    return launch_kernel(sparse_setup_kernel, dim3(p.num_seqs), dim3(kSparseThreads), 0, stream, p);
+}
 
 cudaError_t launch_cascade_setup(const CascadeParams& p, cudaStream_t stream) {
     return launch_kernel(cascade_setup_kernel, dim3(1), dim3(kSetupThreads), 0, stream, p);

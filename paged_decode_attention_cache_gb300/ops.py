@@ -92,6 +92,13 @@ def lib():
         L.pkv_paged_attention_cascade.restype = st
         L.pkv_paged_attention_cascade.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
                                                   _P, _P, _I32, _I32, _P, ctypes.c_size_t, _P, _P]
+        L.pkv_sparse_workspace_bytes.restype = ctypes.c_size_t
+        L.pkv_sparse_workspace_bytes.argtypes = [_I32, _I32, _I32, _I32]
+        L.pkv_paged_attention_sparse.restype = st
+        L.pkv_paged_attention_sparse.argtypes = [_P, ctypes.c_int, _P, ctypes.c_int, _I32, ctypes.c_float, _P, _P,
+                                                 _P, _P, _I32, _P, ctypes.c_size_t, _P, _P]
+        L.pkv_sparse_worthwhile.restype = _I32
+        L.pkv_sparse_worthwhile.argtypes = [_P, _P, _I32, ctypes.c_float]
         L.pkv_cascade_plan.restype = st
         L.pkv_cascade_plan.argtypes = [_P, _P, _I32, _I32, _I32, _I32, _I32, _I32, _P, _P, _P]
         L.pkv_gather_kv_cache.restype = st
@@ -353,6 +360,45 @@ def pkv_paged_attention_cascade(out: torch.Tensor, q: torch.Tensor, scale: float
                                              int(workspace.numel() * workspace.element_size()),
                                              _err_ptr(err_flags), _stream(stream)))
     return out
+
+
+def pkv_sparse_workspace_bytes(num_seqs: int, num_kv_heads: int, head_dim: int, max_pages: int) -> int:
+    return int(lib().pkv_sparse_workspace_bytes(num_seqs, num_kv_heads, head_dim, max_pages))
+
+
+def sparse_workspace(num_seqs: int, num_kv_heads: int, head_dim: int, max_pages: int, device="cuda"):
+    """Caller-side scratch for pkv_paged_attention_sparse (needs no clearing)."""
+    n = pkv_sparse_workspace_bytes(num_seqs, num_kv_heads, head_dim, max_pages)
+    return torch.empty(max(n, 1), dtype=torch.uint8, device=device)
+
+
+def pkv_paged_attention_sparse(out: torch.Tensor, q: torch.Tensor, scale: float, cache: Cache, seqs: Seqs,
+                               page_lists: torch.Tensor, page_counts: torch.Tensor, workspace: torch.Tensor,
+                               err_flags: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Decode attention over the listed logical pages only (device int32
+    page_lists [num_seqs, max_pages], page_counts [num_seqs])."""
+    if page_lists.dtype != torch.int32 or page_counts.dtype != torch.int32:
+        raise ValueError("page_lists / page_counts must be int32")
+    if page_lists.dim() != 2 or page_counts.numel() != page_lists.shape[0]:
+        raise ValueError("page_lists must be [num_seqs, max_pages] and page_counts [num_seqs]")
+    c, s = cache.c_struct(), seqs.c_struct()
+    _check(lib().pkv_paged_attention_sparse(_ptr(out), _DT[out.dtype], _ptr(q), _DT[q.dtype], int(q.shape[1]),
+                                            float(scale), ctypes.byref(c), ctypes.byref(s), _ptr(page_lists),
+                                            _ptr(page_counts), int(page_lists.shape[1]), _ptr(workspace),
+                                            int(workspace.numel() * workspace.element_size()),
+                                            _err_ptr(err_flags), _stream(stream)))
+    return out
+
+
+def pkv_sparse_worthwhile(page_counts: torch.Tensor, context_lens: torch.Tensor, min_sparsity: float) -> bool:
+    """Host policy: use sparse page-indirection when the lists leave out at least
+    min_sparsity of all pages."""
+    pc = page_counts.detach().to("cpu", torch.int32).contiguous()
+    cl = context_lens.detach().to("cpu", torch.int32).contiguous()
+    if pc.numel() != cl.numel():
+        raise ValueError("page_counts and context_lens disagree on num_seqs")
+    return bool(lib().pkv_sparse_worthwhile(ctypes.c_void_p(pc.data_ptr()), ctypes.c_void_p(cl.data_ptr()),
+                                            int(pc.numel()), float(min_sparsity)))
 
 
 def pkv_gather_kv_cache(k_out: torch.Tensor, v_out: torch.Tensor, cu_seq_lens: torch.Tensor, cache: Cache,

@@ -19,6 +19,14 @@ _TORCH = {"f16": torch.float16, "bf16": torch.bfloat16}
 F16_NAN = 0x7E00
 
 
+def cascade_plan_for(w: Workload, min_members: int = 2, min_shared_blocks: int = 8):
+    """The host grouping DecodeStep's cascade schedule uses: items of up to
+    16 / g members (one tensor-core tile of query rows)."""
+    width = max(1, 16 // (w.num_heads // w.num_kv_heads))
+    return ops.pkv_cascade_plan(w.block_tables, w.context_lens, width, min_members=min_members,
+                                min_shared_blocks=min_shared_blocks)
+
+
 class DecodeStep:
     def __init__(self, w: Workload, device: str = "cuda", partition_size: Optional[int] = None,
                  out_dtype: Optional[torch.dtype] = None, schedule: Optional[str] = None,
@@ -27,15 +35,16 @@ class DecodeStep:
         (fixed partitions of partition_size tokens + LSE reduce) or "balanced"
         (equal block ranges per SM, combine fused) or "fused" (balanced, with the
         step's cache write in the same launch) or "cascade" (shared whole-page
-        prefixes read once per group, balanced); by default split when the
-        workload names a partition size, else single."""
+        prefixes read once per group, balanced) or "sparse" (only the workload's
+        listed pages, balanced); by default split when the workload names a
+        partition size, else single."""
         self.w = w
         self.device = device
         dev = torch.device(device)
         self.partition_size = w.partition_size if partition_size is None else partition_size
         if schedule is None:
             schedule = "split" if self.partition_size > 0 else "single"
-        if schedule not in ("single", "split", "balanced", "fused", "cascade"):
+        if schedule not in ("single", "split", "balanced", "fused", "cascade", "sparse"):
             raise ValueError(schedule)
         if schedule != "split":
             self.partition_size = 0
@@ -69,13 +78,18 @@ class DecodeStep:
             self.ws = ops.split_workspace(w.num_rows, w.num_heads, w.head_dim, nparts, device=dev)
         elif schedule in ("balanced", "fused"):
             self.bal_ws = ops.balanced_workspace(w.num_seqs, w.num_kv_heads, w.head_dim, device=dev)
+        elif schedule == "sparse":
+            if w.page_lists is None:
+                raise ValueError("the workload lists no pages")
+            self.page_lists = w.page_lists.to(dev).contiguous()
+            self.page_counts = w.page_counts.to(dev).contiguous()
+            self.sparse_ws = ops.sparse_workspace(w.num_seqs, w.num_kv_heads, w.head_dim,
+                                                  int(self.page_lists.shape[1]), device=dev)
         elif schedule == "cascade":
             if w.q_len != 1:
                 raise ValueError("cascade attention is for q_len 1 decode")
             width = max(1, 16 // (w.num_heads // w.num_kv_heads))
-            members, blocks = ops.pkv_cascade_plan(w.block_tables, w.context_lens, width,
-                                                   min_members=cascade_min_members,
-                                                   min_shared_blocks=cascade_min_shared_blocks)
+            members, blocks = cascade_plan_for(w, cascade_min_members, cascade_min_shared_blocks)
             self.members = members.to(dev).contiguous()
             self.item_blocks = blocks.to(dev).contiguous()
             self.cascade_ws = ops.cascade_workspace(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
@@ -102,6 +116,9 @@ class DecodeStep:
         elif self.schedule == "balanced":
             ops.pkv_paged_attention_balanced(self.out, self.q, self.w.scale, self.cache, self.seqs, self.bal_ws,
                                              self.err, stream)
+        elif self.schedule == "sparse":
+            ops.pkv_paged_attention_sparse(self.out, self.q, self.w.scale, self.cache, self.seqs, self.page_lists,
+                                           self.page_counts, self.sparse_ws, self.err, stream)
         elif self.schedule == "cascade":
             ops.pkv_paged_attention_cascade(self.out, self.q, self.w.scale, self.cache, self.seqs, self.members,
                                             self.item_blocks, self.cascade_ws, self.err, stream)
@@ -127,6 +144,8 @@ class DecodeStep:
         wr = int(self.k_new.shape[0] > 0 and self.schedule != "fused")
         if self.schedule == "cascade":
             return wr + 3   # set-up, attention, reduce
+        if self.schedule == "sparse":
+            return wr + 2   # set-up, attention
         return wr + 1 + int(self.split)
 
     def gather(self, stream=None):

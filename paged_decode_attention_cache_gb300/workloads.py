@@ -57,6 +57,9 @@ class Workload:
     slot_new: Optional[torch.Tensor] = None  # int64 [T]
     partition_size: int = 0                  # 0: single pass
     sliding_window: int = 0                  # 0: every stored token is visible
+    # sparse page-indirection decode: logical pages each sequence attends
+    page_lists: Optional[torch.Tensor] = None   # int32 [B, max_pages]
+    page_counts: Optional[torch.Tensor] = None  # int32 [B]
     block_size: int = BLOCK_SIZE
     v_group: int = 32
     notes: List[str] = field(default_factory=list)
@@ -309,7 +312,44 @@ def cascade_b32_p2048(device="cpu", seed=7, partition_size=512) -> Workload:
                  partition_size=partition_size, prefix_groups=groups, shared_blocks=128, device=device)
 
 
+def sparse_pages(context_lens: List[int], seed: int, sink: int = 4, recent: int = 128,
+                 middle_frac: float = 0.2, max_pages: Optional[int] = None):
+    """Seeded page lists for sparse page-indirection decode: each sequence keeps
+    its first `sink` pages, its last `recent` pages and a uniform random
+    `middle_frac` of the pages between them (sorted, no repeats)."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    npages = [-(-int(c) // BLOCK_SIZE) for c in context_lens]
+    if max_pages is None:
+        max_pages = max([1] + npages)
+    lists = torch.full((len(context_lens), max_pages), -1, dtype=torch.int32)
+    counts = torch.zeros(len(context_lens), dtype=torch.int32)
+    for s, n in enumerate(npages):
+        head = list(range(min(sink, n)))
+        tail = list(range(max(len(head), n - recent), n))
+        mid = list(range(len(head), tail[0] if tail else n))
+        k = int(round(middle_frac * len(mid)))
+        pick = sorted(mid[i] for i in torch.randperm(len(mid), generator=g)[:k].tolist()) if mid else []
+        sel = head + pick + tail
+        lists[s, :len(sel)] = torch.tensor(sel, dtype=torch.int32)
+        counts[s] = len(sel)
+    return lists, counts
+
+
+def sparse_b4_32k(device="cpu", seed=8) -> Workload:
+    """Sparse page-indirection decode at 32K: batch 4, context 32768 (2048 blocks each
+    from an 8192+10% pool), 32/8 heads, head_dim 128, bf16, 1% of tokens with K x 8;
+    each sequence attends its first 4 pages, its last 128 and 20% of the pages
+    between (about 24% of the cache); one new token per sequence."""
+    ctx = [32768] * 4
+    w = build(name="sparse_b4_ctx32k_keep24_h32kv8_d128_bf16", seed=seed, context_lens=ctx, num_heads=32,
+              num_kv_heads=8, head_dim=128, cache="bf16", max_blocks=2048, spike_frac=0.01,
+              spike_scale=8.0, device=device)
+    w.page_lists, w.page_counts = sparse_pages(ctx, seed + 11)
+    return w
+
+
 CONFIGS = {1: tiny_f16, 2: llama3_8b_batch8, 3: long_context_32k, 4: k8v4_batch32,
            5: verify_batch256}
 # workloads beyond the five configurations (rows ranked next)
-EXTRA = {"sliding_window_b8_w4096": sliding_window_b8_w4096, "cascade_b32_p2048": cascade_b32_p2048}
+EXTRA = {"sliding_window_b8_w4096": sliding_window_b8_w4096, "cascade_b32_p2048": cascade_b32_p2048,
+         "sparse_b4_32k": sparse_b4_32k}

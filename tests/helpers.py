@@ -48,10 +48,13 @@ def oracle_cache_after_step(w):
 
 
 def oracle_attention(w, cache_state=None, rows=None, threads=4, partition_size=0,
-                     max_partitions=0, want_out=True):
+                     max_partitions=0, want_out=True, sparse=False):
+    """sparse: attend only the workload's listed pages (page_lists / page_counts)."""
     cs = cache_state or oracle_cache_after_step(w)
     kw = dict(q_len=w.q_len, rows=rows, threads=threads, partition_size=partition_size,
               max_partitions=max_partitions, want_out=want_out, window=w.sliding_window)
+    if sparse:
+        kw.update(page_lists=np_i32(w.page_lists), page_counts=np_i32(w.page_counts))
     if w.cache == "k8v4":
         qc = cs["qc"]
         return oracle.paged_attention(bits(w.q), ODT[w.src_dtype], w.scale, oracle.CACHE_K8V4,
