@@ -99,6 +99,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (ms) over the process group, when
+    there is one with more than one rank; the job's time is its slowest rank's."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world_size, bytes_per_rank_step, ms_per_step):
+    """Whole-job GB/s: every rank moved its own step's bytes in the (max) step time."""
+    return world_size * bytes_per_rank_step / (ms_per_step * 1e-3) / 1e9
+
+
 def make_workload(name, device, seed_offset=0, partition=None):
     from paged_decode_attention_cache_gb300 import workloads as W
     key = WORKLOADS[name]
@@ -354,10 +370,7 @@ def main():
     torch.cuda.synchronize()
     clocks = sampler.stop() if not args.quick else None
     kern_ms = a0.elapsed_time(a1) / (n_attn * n_cycle)
-    t = torch.tensor([step_ms, kern_ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    step_ms, kern_ms = float(t[0]), float(t[1])
+    step_ms, kern_ms = max_over_ranks([step_ms, kern_ms], dev)
     flags = 0
     for st in steps_:
         flags |= st.error_flags()
@@ -409,11 +422,8 @@ def main():
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / Ke
-        te = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        if ws > 1:
-            torch.distributed.all_reduce(te, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(te[0])
-        e2e = {"value": ws * total_b / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+        e2e_ms = max_over_ranks([e2e_ms], dev)[0]
+        e2e = {"value": job_throughput(ws, total_b, e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     peak, peak_src = load_peaks()
@@ -435,7 +445,7 @@ def main():
         torch.distributed.destroy_process_group()
     if rank != 0:
         return 0
-    value = ws * total_b / (step_ms * 1e-3) / 1e9
+    value = job_throughput(ws, total_b, step_ms)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
