@@ -79,6 +79,20 @@ def test_fused_step(cache, H, Hkv, D, ql, new, win):
         check_attention(got, ref, False)
 
 
+def test_fused_step_tiny_free_slot():
+    """The tiny workload's step (its default schedule): one new token written to a
+    slot of a block the sequence does not own, then attention over the 64 tokens;
+    the whole pool bit-exact, then the gather."""
+    w = W.tiny_f16()
+    cs = oracle_cache_after_step(w)
+    ref = oracle_attention(w, cs)
+    st, got = fused(w)
+    check_pool(st, w, cs)
+    check_attention(got, ref, False)
+    st16, got16 = fused(w, torch.float16)
+    check_attention(got16, ref, True)
+
+
 def test_fused_step_llama3_full():
     w = W.llama3_8b_batch8(device="cuda")
     cs = oracle_cache_after_step(w)
