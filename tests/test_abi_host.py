@@ -71,3 +71,66 @@ def test_binding_refuses_to_run_without_the_library(monkeypatch, tmp_path):
     monkeypatch.setattr(ops, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         ops.lib()
+
+
+def _valid_structs(ops, q_len=1, window=0, num_seqs=4, max_blocks=8):
+    """A cache and a batch that pass the host checks; the device addresses are
+    never dereferenced because every call below is refused first."""
+    c = ops._Cache(ops.PKV_CACHE_BF16, 64, 16, 8, 128, 32, 0x10000, 0x20000, None, None, None)
+    s = ops._Seqs(0x30000, 0x40000, num_seqs, max_blocks, q_len, window)
+    return c, s
+
+
+def _cascade(lib, c, s, members=0x50000, blocks=0x60000, items=2, width=4, ws=0x70000, ws_bytes=1 << 30,
+             heads=32):
+    return lib.pkv_paged_attention_cascade(0x80000, 1, 0x90000, 1, heads, ctypes.c_float(0.1), ctypes.byref(c),
+                                           ctypes.byref(s), members, blocks, items, width, ws, ws_bytes, None,
+                                           None)
+
+
+def test_cascade_arguments_checked_on_the_host(lib):
+    from paged_decode_attention_cache_gb300 import ops
+    c, s = _valid_structs(ops, q_len=2)
+    assert _cascade(lib, c, s) == ops.PKV_ERR_UNSUPPORTED and "q_len" in lib.pkv_last_error().decode()
+    c, s = _valid_structs(ops, window=16)
+    assert _cascade(lib, c, s) == ops.PKV_ERR_UNSUPPORTED and "window" in lib.pkv_last_error().decode()
+    c, s = _valid_structs(ops)
+    assert _cascade(lib, c, s, width=5) == ops.PKV_ERR_UNSUPPORTED          # 4 heads x 5 members > 16
+    assert _cascade(lib, c, s, members=None) == ops.PKV_ERR_INVALID_ARG
+    assert _cascade(lib, c, s, items=-1) == ops.PKV_ERR_INVALID_ARG
+    need = lib.pkv_cascade_workspace_bytes(4, 32, 8, 128, 2, 4)
+    assert need > 0
+    assert _cascade(lib, c, s, ws_bytes=need - 1) == ops.PKV_ERR_INVALID_ARG
+    assert "needs" in lib.pkv_last_error().decode()
+    assert _cascade(lib, c, s, ws=0x70010) == ops.PKV_ERR_INVALID_ARG       # not 256-byte aligned
+    assert _cascade(lib, c, s, ws=None) == ops.PKV_ERR_INVALID_ARG
+
+
+def test_cascade_workspace_grows_with_items_and_rows(lib):
+    base = lib.pkv_cascade_workspace_bytes(4, 32, 8, 128, 2, 4)
+    assert lib.pkv_cascade_workspace_bytes(4, 32, 8, 128, 3, 4) >= base
+    assert lib.pkv_cascade_workspace_bytes(8, 32, 8, 128, 2, 4) > base
+    # two fp32 partials (o, max, sum) per row and head are part of it
+    assert base >= 4 * 32 * 2 * (128 + 2) * 4
+    assert lib.pkv_cascade_workspace_bytes(4, 32, 8, 128, 2, 17) == 0
+
+
+def _sparse(lib, c, s, lists=0x50000, counts=0x60000, max_pages=8, ws=0x70000, ws_bytes=1 << 30):
+    return lib.pkv_paged_attention_sparse(0x80000, 1, 0x90000, 1, 32, ctypes.c_float(0.1), ctypes.byref(c),
+                                          ctypes.byref(s), lists, counts, max_pages, ws, ws_bytes, None, None)
+
+
+def test_sparse_arguments_checked_on_the_host(lib):
+    from paged_decode_attention_cache_gb300 import ops
+    c, s = _valid_structs(ops, q_len=4)
+    assert _sparse(lib, c, s) == ops.PKV_ERR_UNSUPPORTED and "q_len" in lib.pkv_last_error().decode()
+    c, s = _valid_structs(ops, window=64)
+    assert _sparse(lib, c, s) == ops.PKV_ERR_UNSUPPORTED
+    c, s = _valid_structs(ops)
+    assert _sparse(lib, c, s, max_pages=0) == ops.PKV_ERR_INVALID_ARG
+    assert _sparse(lib, c, s, lists=None) == ops.PKV_ERR_INVALID_ARG
+    assert _sparse(lib, c, s, counts=None) == ops.PKV_ERR_INVALID_ARG
+    need = lib.pkv_sparse_workspace_bytes(4, 8, 128, 8)
+    assert need == 256 + 256 + lib.pkv_balanced_workspace_bytes(4, 8, 128)   # compacted table + lengths + balanced
+    assert _sparse(lib, c, s, ws_bytes=need - 1) == ops.PKV_ERR_INVALID_ARG
+    assert _sparse(lib, c, s, ws=None) == ops.PKV_ERR_INVALID_ARG
