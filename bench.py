@@ -179,8 +179,9 @@ def traffic_from_profiles(workload, kernel):
 class ClockSampler:
     def __init__(self, device_index):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
-        os.makedirs(os.path.dirname(self.path), exist_ok=True)
+        import tempfile
+        # the raw samples: a scratch file; the JSON line carries their summary
+        self.path = os.path.join(tempfile.gettempdir(), f"pkv_clocks_{os.getpid()}.csv")
         self.device_index = device_index
 
     def start(self):
