@@ -1,7 +1,8 @@
 // attention_impl.cuh -- the persistent paged-attention kernel and its block
-// math, included by attention.cu (attention only) and attention_fused.cu (the
-// decode step that also writes the cache); the two instantiations are
-// compiled side by side.
+// math, included by attention.cu (attention only), attention_fused.cu (the
+// decode step that also writes the cache) and attention_cascade.cu (the
+// cascade pass); the instantiations are compiled side by side.  Short page
+// names in citations ([MTPLX-2], [MLXCEL], ...) are listed at the top of pkv.h.
 //
 // What it computes [metalworking "The KV Cache": the pagedattention kernel,
 // GQA as the stride trick kv_head = q_head / gqa_factor, split-KV decode;
