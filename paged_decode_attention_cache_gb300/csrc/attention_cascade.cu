@@ -1,9 +1,10 @@
-// attention_cascade.cu -- the instantiation of the attention kernel for the two
-// passes of cascade attention [mlxcel manual "KV Cache", §"Paged Decode Storage
-// and Kernels": cascade attention over shared whole-page prefixes]: the suffix
-// pass starts each sequence at its seq_start, the prefix pass reads an item's
-// blocks through its lending member's table and maps the item's query rows to
-// its members.  Compiled apart so that the other kernels carry none of it.
+// attention_cascade.cu -- the instantiation of the attention kernel for the
+// pass of cascade attention [mlxcel manual "KV Cache", §"Paged Decode Storage
+// and Kernels": cascade attention over shared whole-page prefixes]: one
+// balanced pass over a list of items (a group's shared blocks, read through its
+// lending member's table, one query row per member) followed by every sequence
+// from its seq_start on; each entry's combined partial goes to its own slot of
+// the rows it serves.  Compiled apart so that the other kernels carry none of it.
 #include "attention_impl.cuh"
 
 namespace pkv {
