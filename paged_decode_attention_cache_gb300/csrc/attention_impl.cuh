@@ -489,7 +489,7 @@ struct TcMath {
     }
 
     __device__ __forceinline__ void block(const uint8_t* stg, int pos0, int ntok, uint8_t*, int lane) {
-        const int g = lane >> 2, tid = lane & 3;
+        const int tid = lane & 3;
         const uint32_t stg_a = smem_addr(stg);
         float sc[2][4];
 #pragma unroll
