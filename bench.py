@@ -249,8 +249,9 @@ def cpu_baseline(w, attn_bytes, budget_s, split=False, sparse=False):
             break
     per = el / n
     return {"value": attn_bytes / per / 1e9, "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{n} full attention step(s) of {w.name} (fp64 scalar oracle: split-KV partials "
-                      f"+ LSE reduce when the step splits), {per:.3f} s each", "seconds_per_step": per}
+            "sample": f"{n} full attention step(s) of {w.name} (fp64 scalar oracle"
+                      + (": the listed pages only" if sparse else ": split-KV partials + LSE reduce" if split else "")
+                      + f"), {per:.3f} s each", "seconds_per_step": per}
 
 
 def run_reference(args):
