@@ -129,3 +129,15 @@ def test_cascade_serving_shape_sampled():
     st, got = run_cascade(w, min_shared=8)
     assert st.members.shape[0] == 8
     check_attention(got[rows], ref[rows], False)
+
+
+def test_cascade_empty_and_one_token_sequences():
+    # sequences with no token and with one token next to a shared group
+    ctx = [0, 1, 81, 90, 100]
+    w = W.build(name="t", seed=760, context_lens=ctx, num_heads=8, num_kv_heads=2, head_dim=64, cache="f16",
+                prefix_groups=[[2, 3, 4]], shared_blocks=5, new_tokens="none")
+    ref = oracle_attention(w, threads=8)
+    st, got = run_cascade(w)
+    assert st.members.shape[0] == 1
+    assert np.array_equal(got[0], np.zeros_like(got[0]))
+    check_attention(got, ref, False)

@@ -137,3 +137,17 @@ def test_sparse_32k_sampled():
     st, got = run_sparse(w)
     assert st.error_flags() == 0
     check_attention(got, ref, False)
+
+
+def test_sparse_empty_context_and_single_token():
+    ctx = [0, 1, 33]
+    w = W.build(name="t", seed=860, context_lens=ctx, num_heads=8, num_kv_heads=2, head_dim=64, cache="bf16",
+                new_tokens="none")
+    w.page_lists = torch.tensor([[0, 1, -1], [0, -1, -1], [0, 2, -1]], dtype=torch.int32)
+    w.page_counts = torch.tensor([2, 1, 2], dtype=torch.int32)
+    ref = oracle_attention(w, threads=8, sparse=True)
+    st, got = run_sparse(w)
+    # sequence 0 lists pages it does not have: skipped and flagged, zeros out
+    assert st.error_flags() & PKV_DEVERR_PAGE_LIST
+    assert np.array_equal(got[0], np.zeros_like(got[0]))
+    check_attention(got, ref, False)
