@@ -401,8 +401,9 @@ pkv_status pkv_paged_attention_balanced_noalloc(void *out, pkv_dtype out_dtype, 
                                                 const pkv_seqs *seqs, uint32_t *err_flags, pkv_stream_t stream);
 
 /*
- * Copy every visible token of every sequence back to contiguous storage
- * [METAL names the gather_kv_cache kernel].
+ * Copy every stored token of every sequence (all context_lens[s] of them; a
+ * sliding window does not apply) back to contiguous storage [METAL names the
+ * gather_kv_cache kernel].
  *   cu_seq_lens  int32 [num_seqs + 1] device: cu[0] = 0, cu[s+1] = cu[s] + context_lens[s].
  *   k_out, v_out [cu[num_seqs], num_kv_heads, head_dim] in the cache dtype
  *                (PKV_CACHE_F16 or PKV_CACHE_BF16 caches only).
