@@ -19,7 +19,10 @@
  *           row-major in the shape documented beside it, and 16-byte aligned.
  *           The library allocates nothing on the device and keeps no state
  *           between calls; split-KV scratch is sized by
- *           pkv_split_workspace_bytes() and passed in by the caller.
+ *           pkv_split_workspace_bytes() and passed in by the caller.  The one
+ *           exception is pkv_paged_attention_balanced_noalloc: its scratch is
+ *           a static device array inside the library image that keeps the
+ *           last call's contents (see its declaration for the rules).
  * Streams.  Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL
  *           is the legacy default stream).  The return value only reports the
  *           host-side argument checks and the launch itself.
@@ -31,7 +34,9 @@
  *           up) never trap: the affected token is skipped and a PKV_DEVERR_*
  *           bit is OR-ed into `*err_flags` when err_flags is non-NULL
  *           (caller-owned device uint32, zeroed by the caller).
- * Threads.  Stateless: calls may be made concurrently from several threads.
+ * Threads.  Stateless: calls may be made concurrently from several threads,
+ *           except pkv_paged_attention_balanced_noalloc, whose calls share one
+ *           array per device and must not overlap on the GPU.
  * Shapes.   block_size must be 16, head_dim 64 or 128, num_heads a multiple of
  *           num_kv_heads with a group size num_heads/num_kv_heads in
  *           {1, 2, 4, 8}.
@@ -386,8 +391,11 @@ pkv_status pkv_cascade_plan(const int32_t *block_tables, const int32_t *context_
  *   not exceed PKV_NOALLOC_SCRATCH_BYTES (about 3000 (sequence, kv head) pairs
  *   at head_dim 128, 6900 at head_dim 64); a larger batch returns
  *   PKV_ERR_INVALID_ARG with an explanation and launches nothing.
- *   Set-up: the first call on a device (with that device current) looks up the
- *   array's device address; make that first call before any stream capture.
+ *   Set-up: a call made while `stream` is not being captured looks up the
+ *   array's device address in the current context (cudaGetSymbolAddress) and
+ *   remembers it; a call made during stream capture uses the remembered
+ *   address, so make the first call in each context (and the first after a
+ *   cudaDeviceReset) before any capture, or it returns PKV_ERR_INVALID_ARG.
  *   Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents; each call clears the part that must start at zero (one
  *   cudaMemsetAsync on `stream`, no allocation).  Calls that overlap on the GPU

@@ -643,41 +643,83 @@ pkv_status pkv_decode_step_balanced(void* out, pkv_dtype out_dtype, const void* 
 // own device image, so a caller that cannot allocate device memory still gets
 // the balanced schedule.  Every GPU that loads the library holds it until the
 // process exits.  Host code must not use the symbol as a device address; the
-// address is looked up once per device below.
+// address is looked up with the caller's device current (noalloc_scratch).
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(PKV_NOALLOC_SCRATCH_BYTES);
 static_assert(kNoAllocScratchBytes % 256 == 0, "scratch size must keep 256-byte alignment");
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 256;
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
-// Device address of g_noalloc_scratch on the current device, looked up on the
-// first call made with that device current (cudaGetSymbolAddress).
-void* noalloc_scratch(pkv_status* st) {
+// cuCtxGetCurrent from the driver, fetched once through the runtime.
+CtxGetCurrentFn ctx_get_current_fn() {
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(f);
+    });
+    return fn;
+}
+
+// Device address of g_noalloc_scratch in the current context.  A call made
+// while `stream` is not being captured looks the address up afresh
+// (cudaGetSymbolAddress, with the caller's device current) and remembers it for
+// that context; a call made during stream capture uses the remembered address,
+// so the first call in a context must come before any capture.  Looking it up
+// again on every uncaptured call keeps a cached address from outliving its
+// module: after cudaDeviceReset, or in another context on the same device, the
+// array sits at a different address.
+void* noalloc_scratch(cudaStream_t stream, pkv_status* st) {
+    constexpr int kSlots = 64;
     static std::mutex mu;
-    static void* addr[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        *st = fail(PKV_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    static CUcontext ctxs[kSlots] = {};
+    static void* addrs[kSlots] = {};
+    static int next = 0;
+    auto get_ctx = ctx_get_current_fn();
+    if (!get_ctx) {
+        *st = fail(PKV_ERR_CUDA, "cuCtxGetCurrent is unavailable from the driver");
         return nullptr;
     }
-    if (dev < 0 || dev >= kMaxDevices) {
-        *st = fail(PKV_ERR_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxDevices - 1);
-        return nullptr;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        cap = cudaStreamCaptureStatusActive;   // treat an unanswerable query as capture: no look-up
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* ptr = nullptr;
-        e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+        const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
         if (e != cudaSuccess || ptr == nullptr) {
             *st = fail(PKV_ERR_CUDA, "cudaGetSymbolAddress of the static scratch: %s", cudaGetErrorString(e));
             return nullptr;
         }
-        addr[dev] = ptr;
+        CUcontext ctx = nullptr;
+        if (get_ctx(&ctx) == CUDA_SUCCESS && ctx != nullptr) {
+            int slot = -1;
+            for (int i = 0; i < kSlots; ++i)
+                if (ctxs[i] == ctx) slot = i;
+            if (slot < 0) {
+                slot = next;
+                next = (next + 1) % kSlots;
+                ctxs[slot] = ctx;
+            }
+            addrs[slot] = ptr;
+        }
+        return ptr;
     }
-    return addr[dev];
+    CUcontext ctx = nullptr;
+    if (get_ctx(&ctx) == CUDA_SUCCESS && ctx != nullptr)
+        for (int i = 0; i < kSlots; ++i)
+            if (ctxs[i] == ctx) return addrs[i];
+    *st = fail(PKV_ERR_INVALID_ARG,
+               "the first pkv_paged_attention_balanced_noalloc call in a context must come before stream capture "
+               "(it looks up the static scratch's device address)");
+    return nullptr;
 }
 
 }  // namespace
@@ -704,7 +746,7 @@ pkv_status pkv_paged_attention_balanced_noalloc(void* out, pkv_dtype out_dtype, 
                     "batch too large for the static scratch: %d sequences x %d kv heads at head_dim %d need %zu "
                     "bytes, the library holds %zu (use pkv_paged_attention_balanced with your own workspace)",
                     seqs->num_seqs, cache->num_kv_heads, cache->head_dim, need, kNoAllocScratchBytes);
-    void* ws = noalloc_scratch(&st);
+    void* ws = noalloc_scratch(reinterpret_cast<cudaStream_t>(stream), &st);
     if (!ws) return st;
     const size_t pairs = size_t(seqs->num_seqs) * size_t(cache->num_kv_heads);
     const size_t slots = size_t(pkv::kMaxGrid) + pairs;
