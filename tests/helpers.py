@@ -1,65 +1,57 @@
-"""Shared test plumbing: moving seeded workloads into the oracle's numpy form.
+"""Shared test plumbing: the oracle's workload adapter (oracle.from_workload)
+under the names the tests use, the oracle thread count, and guard bands around
+GPU output buffers.  Nothing here computes attention or quantises."""
+import os
 
-Nothing here computes attention or quantises: it converts tensors to raw bits
-and calls the oracle."""
-import numpy as np
 import torch
 
-import oracle
-
-ODT = {"f16": oracle.F16, "bf16": oracle.BF16}
-OCACHE = {"f16": oracle.CACHE_F16, "bf16": oracle.CACHE_BF16, "k8v4": oracle.CACHE_K8V4}
-
-
-def bits(t: torch.Tensor) -> np.ndarray:
-    """Raw 16-bit patterns of an fp16/bf16 tensor as numpy uint16 (host copy)."""
-    t = t.detach().cpu().contiguous()
-    assert t.element_size() == 2
-    return t.view(torch.int16).numpy().view(np.uint16).copy()
+from oracle.from_workload import ODT, OCACHE, bits, np_i32, np_i64  # noqa: F401
+from oracle.from_workload import attention as oracle_attention  # noqa: F401
+from oracle.from_workload import cache_after_step as oracle_cache_after_step  # noqa: F401
 
 
-def np_i32(t):
-    return t.detach().cpu().contiguous().to(torch.int32).numpy().copy()
+# oracle threads for full-size comparisons: every host core
+ALL_CORES = os.cpu_count() or 8
+
+GUARD_BYTES = 4096
+# quiet-NaN patterns written into a guarded buffer (output and bands alike)
+_CANARY = {torch.float32: (torch.int32, 0x7FC0DEAD), torch.float16: (torch.int16, 0x7E5A),
+           torch.bfloat16: (torch.int16, 0x7FDA)}
 
 
-def np_i64(t):
-    return t.detach().cpu().contiguous().to(torch.int64).numpy().copy()
+class GuardedOut:
+    """An output buffer with GUARD_BYTES of canary bytes on each side.
+
+    The output and both bands start as a NaN bit pattern, so an element the
+    kernel never writes stays NaN (and fails parity) and a write past either end
+    of the output changes a band; check() asserts both bands are untouched."""
+
+    def __init__(self, shape, dtype, device):
+        ity, pat = _CANARY[dtype]
+        esz = torch.empty((), dtype=dtype).element_size()
+        self.g = GUARD_BYTES // esz
+        self.n = 1
+        for x in shape:
+            self.n *= int(x)
+        self.pattern = pat
+        self.buf = torch.full((self.n + 2 * self.g,), pat, dtype=ity, device=device).view(dtype)
+        self.out = self.buf[self.g:self.g + self.n].view(tuple(shape))
+
+    def refill(self):
+        ity, _ = _CANARY[self.out.dtype]
+        self.buf.view(ity).fill_(self.pattern)
+
+    def check(self):
+        ity, _ = _CANARY[self.out.dtype]
+        raw = self.buf.view(ity)
+        head, tail = raw[:self.g], raw[self.g + self.n:]
+        bad = int((head != self.pattern).sum()) + int((tail != self.pattern).sum())
+        assert bad == 0, f"{bad} guard-band elements around the output were overwritten"
 
 
-def oracle_cache_after_step(w):
-    """The oracle's own cache state after the step's write, built from the
-    workload's inputs by the oracle's write routines."""
-    if w.cache in ("f16", "bf16"):
-        kc, vc = bits(w.k_cache), bits(w.v_cache)
-        if w.k_new is not None and w.k_new.shape[0]:
-            oracle.reshape_and_cache(kc, vc, bits(w.k_new), bits(w.v_new), np_i64(w.slot_new))
-        return {"k": kc, "v": vc}
-    qc = oracle.QuantCache(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.v_group)
-    nan16 = np.uint16(0x7e00)
-    qc.k_scale[:] = nan16       # unused slots poison any stray read
-    qc.v_scale[:] = nan16
-    qc.v_zero[:] = nan16
-    odt = ODT[w.src_dtype]
-    if w.k_hist is not None and w.k_hist.shape[0]:
-        oracle.quantize_kv(qc, bits(w.k_hist), bits(w.v_hist), odt, np_i64(w.slot_hist))
-    if w.k_new is not None and w.k_new.shape[0]:
-        oracle.quantize_kv(qc, bits(w.k_new), bits(w.v_new), odt, np_i64(w.slot_new))
-    return {"qc": qc}
-
-
-def oracle_attention(w, cache_state=None, rows=None, threads=4, partition_size=0,
-                     max_partitions=0, want_out=True, sparse=False):
-    """sparse: attend only the workload's listed pages (page_lists / page_counts)."""
-    cs = cache_state or oracle_cache_after_step(w)
-    kw = dict(q_len=w.q_len, rows=rows, threads=threads, partition_size=partition_size,
-              max_partitions=max_partitions, want_out=want_out, window=w.sliding_window)
-    if sparse:
-        kw.update(page_lists=np_i32(w.page_lists), page_counts=np_i32(w.page_counts))
-    if w.cache == "k8v4":
-        qc = cs["qc"]
-        return oracle.paged_attention(bits(w.q), ODT[w.src_dtype], w.scale, oracle.CACHE_K8V4,
-                                      qc.k_q, qc.v_q, np_i32(w.block_tables),
-                                      np_i32(w.context_lens), k_scale=qc.k_scale,
-                                      v_scale=qc.v_scale, v_zero=qc.v_zero, v_group=qc.v_group, **kw)
-    return oracle.paged_attention(bits(w.q), ODT[w.src_dtype], w.scale, OCACHE[w.cache], cs["k"],
-                                  cs["v"], np_i32(w.block_tables), np_i32(w.context_lens), **kw)
+def guard(st):
+    """Give a DecodeStep a guarded output buffer (same shape and dtype); returns
+    the guard, whose check() the caller runs after the step."""
+    g = GuardedOut(st.out.shape, st.out.dtype, st.out.device)
+    st.out = g.out
+    return g

@@ -13,7 +13,7 @@ import torch
 import oracle
 from paged_decode_attention_cache_gb300 import ops, workloads as W
 from paged_decode_attention_cache_gb300.runner import DecodeStep
-from tests.helpers import bits, np_i32, np_i64, oracle_attention, oracle_cache_after_step
+from tests.helpers import ALL_CORES, bits, guard, np_i32, np_i64, oracle_attention, oracle_cache_after_step
 
 pytestmark = pytest.mark.gpu
 
@@ -50,9 +50,11 @@ def run_step(w, partition=None, out_dtype=torch.float32):
         st = DecodeStep(w, "cuda", out_dtype=out_dtype, schedule="balanced")
     else:
         st = DecodeStep(w, "cuda", partition_size=partition, out_dtype=out_dtype)
+    g = guard(st)
     out = st.step()
     torch.cuda.synchronize()
     assert st.error_flags() == 0, f"device error flags {st.error_flags():#x}"
+    g.check()
     return st, out.double().cpu().numpy()
 
 
@@ -111,7 +113,7 @@ def test_half_and_bf16_outputs():
 def test_llama3_8b_batch8_full():
     w = W.llama3_8b_batch8(device="cuda")
     cs = oracle_cache_after_step(w)
-    ref = oracle_attention(w, cs, threads=8)
+    ref = oracle_attention(w, cs, threads=ALL_CORES)
     for part in (256, 0, "bal"):
         st, got = run_step(w, part)
         check_attention(got, ref, False)
@@ -125,7 +127,7 @@ def test_long_context_32k_split_and_partials():
     w = W.long_context_32k(device="cuda")
     cs = oracle_cache_after_step(w)
     NP = w.max_partitions
-    ref, (po, pm, pl) = oracle_attention(w, cs, threads=8, partition_size=512, max_partitions=NP)
+    ref, (po, pm, pl) = oracle_attention(w, cs, threads=ALL_CORES, partition_size=512, max_partitions=NP)
     st, got = run_step(w, 512)
     check_attention(got, ref, False)
     tmp, ml, es = (t.double().cpu().numpy() for t in st.ws)
@@ -138,7 +140,7 @@ def test_long_context_32k_split_and_partials():
 
 def test_long_context_32k_balanced():
     w = W.long_context_32k(device="cuda")
-    ref = oracle_attention(w, threads=8)
+    ref = oracle_attention(w, threads=ALL_CORES)
     _, got = run_step(w, "bal")
     check_attention(got, ref, False)
 

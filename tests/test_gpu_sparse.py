@@ -10,7 +10,7 @@ import torch
 
 from paged_decode_attention_cache_gb300 import ops, workloads as W
 from paged_decode_attention_cache_gb300.runner import DecodeStep
-from tests.helpers import oracle_attention, oracle_cache_after_step
+from tests.helpers import guard, oracle_attention, oracle_cache_after_step
 from tests.test_gpu_parity import check_attention
 
 pytestmark = pytest.mark.gpu
@@ -60,8 +60,10 @@ def poison_unlisted(w):
 
 def run_sparse(w):
     st = DecodeStep(w, "cuda", out_dtype=torch.float32, schedule="sparse")
+    g = guard(st)
     out = st.step()
     torch.cuda.synchronize()
+    g.check()
     return st, out.double().cpu().numpy()
 
 
@@ -130,7 +132,7 @@ def test_sparse_long_sequences_many_pages():
     check_attention(got, ref, False)
 
 
-def test_sparse_32k_sampled():
+def test_sparse_32k_full():
     """The bench's sparse workload (batch 4 at 32K, a quarter of the pages)."""
     w = W.sparse_b4_32k(device="cpu")
     ref = oracle_attention(w, threads=16, sparse=True)

@@ -11,7 +11,7 @@ import torch
 
 from paged_decode_attention_cache_gb300 import ops, workloads as W
 from paged_decode_attention_cache_gb300.runner import DecodeStep
-from tests.helpers import bits, oracle_attention, oracle_cache_after_step
+from tests.helpers import ALL_CORES, bits, guard, oracle_attention, oracle_cache_after_step
 from tests.test_gpu_parity import check_attention
 
 pytestmark = pytest.mark.gpu
@@ -32,9 +32,11 @@ def run(w, part, out_dtype=torch.float32):
         st = DecodeStep(w, "cuda", out_dtype=out_dtype, schedule="balanced")
     else:
         st = DecodeStep(w, "cuda", partition_size=part, out_dtype=out_dtype)
+    g = guard(st)
     out = st.step()
     torch.cuda.synchronize()
     assert st.error_flags() == 0, f"device error flags {st.error_flags():#x}"
+    g.check()
     return st, out.double().cpu().numpy()
 
 
@@ -60,22 +62,22 @@ def test_verify_small(D, H, Hkv, ql, dt, part):
     check_attention(got, ref, False)
 
 
-def test_verify_batch256_full_sampled_rows():
+def test_verify_batch256_full():
+    """The serving-scale verify batch at full size: all 256 x 4 rows on the
+    balanced, split and single-pass schedules (the oracle on every host core)."""
     w = W.verify_batch256(device="cuda")
     st, got = run(w, "bal")
     cs = oracle_cache_after_step(w)
     # the drafts' K/V were written by the step: whole pool bit-exact
     assert np.array_equal(bits(st.cache.k), cs["k"]) and np.array_equal(bits(st.cache.v), cs["v"])
-    rng = np.random.default_rng(0)
-    seqs = np.concatenate([[int(np.argmax(w.context_lens.cpu())), int(np.argmin(w.context_lens.cpu()))],
-                           rng.choice(w.num_seqs, 14, replace=False)])
-    rows = sorted({int(s) * 4 + j for s in seqs for j in range(4)})
-    ref = oracle_attention(w, cs, rows=rows, threads=16)
-    check_attention(got[rows], ref[rows], False)
+    del st
+    ref = oracle_attention(w, cs, threads=ALL_CORES)
+    del cs
+    check_attention(got, ref, False)
     _, got16 = run(w, 512, torch.bfloat16)
-    check_attention(got16[rows], ref[rows], True)
+    check_attention(got16, ref, True)
     _, got_single = run(w, 0)
-    check_attention(got_single[rows], ref[rows], False)
+    check_attention(got_single, ref, False)
 
 
 # ---------------------------------------------------------------- K8/V4
@@ -112,14 +114,14 @@ def test_k8v4_fp16_queries():
     assert np.abs(got - ref).max() <= K8V4_ABS
 
 
-def test_k8v4_batch32_full_sampled_rows():
+def test_k8v4_batch32_full():
+    """The K8/V4 batch at full size, all 32 rows, on the split, single-pass and
+    balanced schedules."""
     w = W.k8v4_batch32(device="cuda")
-    st, got = run(w, 512)
     cs = oracle_cache_after_step(w)
-    rows = sorted(set([0, 31, int(np.argmax(w.context_lens.cpu()))] + list(range(3, 32, 5))))
-    ref = oracle_attention(w, cs, rows=rows, threads=16)
-    err = np.abs(got[rows] - ref[rows]).max()
-    assert err <= K8V4_ABS, f"max abs err {err:.3e}"
-    for part in (0, "bal"):
-        _, got1 = run(w, part)
-        assert np.abs(got1[rows] - ref[rows]).max() <= K8V4_ABS
+    ref = oracle_attention(w, cs, threads=ALL_CORES)
+    for part in (512, 0, "bal"):
+        _, got = run(w, part)
+        assert np.isfinite(got).all()
+        err = np.abs(got - ref).max()
+        assert err <= K8V4_ABS, f"max abs err {err:.3e} (schedule {part})"

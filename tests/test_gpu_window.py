@@ -11,7 +11,7 @@ import torch
 
 from paged_decode_attention_cache_gb300 import ops, workloads as W
 from paged_decode_attention_cache_gb300.runner import DecodeStep
-from tests.helpers import oracle_attention, oracle_cache_after_step
+from tests.helpers import ALL_CORES, oracle_attention, oracle_cache_after_step
 from tests.test_gpu_parity import check_attention, run_step
 
 pytestmark = pytest.mark.gpu
@@ -93,14 +93,14 @@ def test_window_split_partials_inside_the_window():
     check_attention(st.out.double().cpu().numpy(), ref, False)
 
 
-def test_window_workload_sampled_rows():
+def test_window_workload_full():
+    """The sliding-window workload at full size, every row, balanced and split."""
     w = W.sliding_window_b8_w4096(device="cuda")
     st, got = run_step(w, "bal")
-    rows = [0, 3, 5, 7]
-    ref = oracle_attention(w, rows=rows, threads=16)
-    check_attention(got[rows], ref[rows], False)
+    ref = oracle_attention(w, threads=ALL_CORES)
+    check_attention(got, ref, False)
     _, got_split = run_step(w, 512)
-    check_attention(got_split[rows], ref[rows], False)
+    check_attention(got_split, ref, False)
 
 
 def test_negative_window_is_rejected():
