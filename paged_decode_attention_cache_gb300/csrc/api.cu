@@ -218,7 +218,7 @@ pkv_status attn_setup(pkv::AttnParams* p, const void* q, pkv_dtype q_dtype, int3
 }
 
 pkv_status attn_launch(pkv::AttnParams p, const pkv_cache* cache, int gqa, pkv_stream_t stream) {
-    const bool tc = pkv::attention_uses_tensor_cores(cache->kind, p.q_len, pkv::is_cascade_pass(p));
+    const bool tc = pkv::attention_uses_tensor_cores(cache->kind, p.q_len, gqa, pkv::is_cascade_pass(p));
     CUtensorMap km, vm;
     pkv_status st = cache_maps(cache, &km, &vm, tc);
     if (st != PKV_OK) return st;

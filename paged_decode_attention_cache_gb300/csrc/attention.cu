@@ -9,12 +9,17 @@ namespace pkv {
 bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len) {
     const bool shape = (head_dim == 64 || head_dim == 128) && (gqa == 1 || gqa == 2 || gqa == 4 || gqa == 8);
     if (!shape || q_len < 1) return false;
-    if (attention_uses_tensor_cores(cache_kind, q_len)) return gqa * q_len <= kMaxRows;
+    if (attention_uses_tensor_cores(cache_kind, q_len, gqa)) return gqa * q_len <= kMaxRows;
     return cache_kind == PKV_CACHE_F16 || cache_kind == PKV_CACHE_BF16;
 }
 
-bool attention_uses_tensor_cores(int cache_kind, int q_len, bool cascade_pass) {
-    return cascade_pass || q_len > 1 || cache_kind == PKV_CACHE_K8V4;
+// The CUDA-core math spends ~500 warp instructions per 16-token block at group
+// size 4 and is latency-bound below the HBM rate (~36 GB/s per SM with 11
+// consumer warps, slower with fewer); the MMA formulation needs ~150 and
+// streams at ~42 GB/s per SM.  At group size 1 and 2 the CUDA-core math does
+// proportionally less work and is a little faster (both measured).
+bool attention_uses_tensor_cores(int cache_kind, int q_len, int gqa, bool cascade_pass) {
+    return cascade_pass || cache_kind == PKV_CACHE_K8V4 || q_len > 1 || gqa * q_len >= kTcMinRows;
 }
 
 cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& km, const CUtensorMap& vm,

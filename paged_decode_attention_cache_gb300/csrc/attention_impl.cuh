@@ -35,9 +35,11 @@
 // segment while the producer already streams the next one.
 //
 // Block math:
-//   CcMath  fp16/bf16, q_len 1, CUDA cores: fp32 q pairs, packed fma.rn.f32x2,
-//           reduce-scatter shuffles, softmax over 16 x g scores in shared memory;
-//   TcMath  fp16/bf16 verify blocks (q_len > 1): mma.sync m16n8k16 on 16 query
+//   CcMath  fp16/bf16 decode at group size 1 or 2, CUDA cores: fp32 q pairs,
+//           packed fma.rn.f32x2, reduce-scatter shuffles, softmax over 16 x g
+//           scores in shared memory;
+//   TcMath  fp16/bf16 whenever a kv head serves >= 4 query rows (decode at
+//           group size 4 and 8, verify blocks): mma.sync m16n8k16 on 16 query
 //           rows (g heads x q_len drafts), 128B-swizzled tiles via ldmatrix;
 //   TqMath  K8/V4, any q_len: the contraction turned around (S^T = K Q^T,
 //           O^T = V^T P^T) so the query columns sit on the MMA's N side; codes
@@ -205,9 +207,8 @@ struct CcMath {
     static constexpr bool kTensor = false;
     static constexpr int kD = D;
     // 11 consumer warps + the producer: 12 warps, three per SM sub-partition,
-    // which leaves 168 registers a thread -- enough for this math up to g = 4;
-    // g = 8 keeps 16 heads' q and accumulators and takes 7 (255 registers)
-    static constexpr int NCW = G >= 8 ? 7 : 11;
+    // which leaves 168 registers a thread (this math runs group sizes 1 and 2)
+    static constexpr int NCW = 11;
     static constexpr int CH = D / 8;                               // 16-byte chunks per row
     static constexpr int LPT = (G * D / 64 > 8) ? G * D / 64 : 8;  // lanes per token (QK)
     static constexpr int TPP = 32 / LPT;                           // tokens per pass
@@ -1068,7 +1069,9 @@ struct SegIter {
 // more segment), then cuts the list's total cost into nlanes equal ranges, so a
 // CTA whose range starts a sequence is given fewer blocks.  Unit u of sequence s
 // sits at cost position u + seg_cost * (r_s + 1), r_s = non-empty sequences
-// before s; CTA k serves cost range [k * chunk, (k + 1) * chunk).
+// before s.  The first sequence's charge lies before every range (a CTA that
+// starts with it has no extra segment): CTA k serves cost range
+// [seg_cost + k * chunk, seg_cost + (k + 1) * chunk).
 struct Plan {
     long long u0, u1, chunk, start0;
     int s0, ctx0, r0;
@@ -1134,9 +1137,12 @@ __device__ void cta_plan(const AttnParams& p, int lane_idx, int nlanes, long lon
     SeqPos mine{};
     for (int r0 = 0; r0 < B; r0 += nthr) mine = plan_round<CASC>(p, r0, red, base);
     const long long total_u = (long long)(base & 0xffffffffull), total_c = (long long)(base >> 32);
-    long long chunk = (total_c + nlanes - 1) / nlanes;
+    // split mode charges nothing (seg_cost 0)
+    const long long span = total_c > p.seg_cost ? total_c - p.seg_cost : 0;
+    long long chunk = (span + nlanes - 1) / nlanes;
     if (p.mode == kModeBalanced && chunk < p.min_chunk + p.seg_cost) chunk = p.min_chunk + p.seg_cost;
-    const long long X0 = lane_idx * chunk, X1 = X0 + chunk;
+    if (chunk < 1) chunk = 1;
+    const long long X0 = p.seg_cost + lane_idx * chunk, X1 = X0 + chunk;
     if (threadIdx.x == 0) {
         flag[0] = B;         // s0
         flag[2] = 0;         // ctx0
@@ -1570,80 +1576,77 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             }
         }
         if (piece) {
-            // the last piece of a pair to finish combines all of them (no waiting)
-            __threadfence();
+            // The last piece of a pair to finish combines all of them (no
+            // waiting).  Publication: every thread's partial stores, the barrier,
+            // then one gpu-scope fence and the count by thread 0 (the barrier
+            // makes the other threads' stores part of what the fence releases).
             named_barrier_sync(1, CT);
-            const int c_lo = int((sg.pair_start + sg.cost_base) / chunk),
-                      c_hi = int((sg.pair_start + sg.nu - 1 + sg.cost_base) / chunk);
+            const int c_lo = int((sg.pair_start + sg.cost_base - p.seg_cost) / chunk),
+                      c_hi = int((sg.pair_start + sg.nu - 1 + sg.cost_base - p.seg_cost) / chunk);
             const int np = c_hi - c_lo + 1;
             if (tid == 0) {
+                __threadfence();
                 const int prev = atomicAdd(&p.counters[pair], 1);
+                __threadfence();   // acquire: the other pieces' partials before our loads
                 flag[1] = (prev == np - 1) ? 1 : 0;
             }
             named_barrier_sync(1, CT);
             if (flag[1]) {
-                __threadfence();
                 // Pieces hold unnormalised sums relative to their own max m_c:
-                // O = sum_c 2^(m_c - M) O_c, L = sum_c 2^(m_c - M) l_c.  Four pieces
-                // at a time, each with its (m, l) and its slice of O loaded in the
-                // same round trip, folded in by an online rescale.
-                float4 acc[kPer];
-                float Mr[kPer], Lr[kPer];
-#pragma unroll
-                for (int k = 0; k < kPer; ++k) {
-                    acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    Mr[k] = -INFINITY;
-                    Lr[k] = 0.f;
-                }
-                for (int c = 0; c < np; c += 4) {
-                    float2 ml[kPer][4];
-                    float4 v[kPer][4];
-#pragma unroll
-                    for (int k = 0; k < kPer; ++k) {
-                        const int i4 = tid + k * CT;
-                        const int m = i4 < n4 ? (i4 << 2) / D : 0;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            ml[k][u] = make_float2(-INFINITY, 0.f);
-                            v[k][u] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            if (i4 < n4 && c + u < np) {
-                                const size_t sl = size_t((c_lo + c + u + sg.s) * Hkv + sg.kvh) * kMaxRows;
-                                ml[k][u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl + m);
-                                v[k][u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * D) + i4);
-                            }
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < kPer; ++k) {
-                        float Mn = Mr[k];
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            if (ml[k][u].y > 0.f) Mn = fmaxf(Mn, ml[k][u].x);
-                        const float a = (Mr[k] == -INFINITY) ? 0.f : exp2f(Mr[k] - Mn);
-                        acc[k].x *= a; acc[k].y *= a; acc[k].z *= a; acc[k].w *= a;
-                        Lr[k] *= a;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const float f = (ml[k][u].y > 0.f) ? exp2f(ml[k][u].x - Mn) : 0.f;
-                            acc[k].x = fmaf(f, v[k][u].x, acc[k].x);
-                            acc[k].y = fmaf(f, v[k][u].y, acc[k].y);
-                            acc[k].z = fmaf(f, v[k][u].z, acc[k].z);
-                            acc[k].w = fmaf(f, v[k][u].w, acc[k].w);
-                            Lr[k] = fmaf(f, ml[k][u].y, Lr[k]);
-                        }
-                        Mr[k] = Mn;
-                    }
-                }
+                // O = sum_c 2^(m_c - M) O_c, L = sum_c 2^(m_c - M) l_c.  The pieces'
+                // (m, l) and O slices are loaded eight at a time, all in flight
+                // together, and folded in by an online rescale in piece order (so
+                // the result does not depend on which CTA combines); this CTA's own
+                // piece comes from its registers, not from memory.
+                const int own = lane_idx - c_lo;
+                constexpr int kFly = 8;
 #pragma unroll
                 for (int k = 0; k < kPer; ++k) {
                     const int i4 = tid + k * CT;
-                    if (i4 >= n4) continue;
+                    if (i4 >= n4) break;
                     const int m = (i4 << 2) / D, d = (i4 << 2) - m * D;
-                    const float L = Lr[k];
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                    float Mr = -INFINITY, Lr = 0.f;
+                    for (int c0 = 0; c0 < np; c0 += kFly) {
+                        float2 ml[kFly];
+                        float4 v[kFly];
+#pragma unroll
+                        for (int u = 0; u < kFly; ++u) {
+                            ml[u] = make_float2(-INFINITY, 0.f);
+                            v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            const int c = c0 + u;
+                            if (c == own) {
+                                ml[u] = make_float2(resM[k], resL[k]);
+                                v[u] = res[k];
+                            } else if (c < np) {
+                                const size_t sl = size_t((c_lo + c + sg.s) * Hkv + sg.kvh) * kMaxRows;
+                                ml[u] = __ldcg(reinterpret_cast<const float2*>(p.part_ml) + sl + m);
+                                v[u] = __ldcg(reinterpret_cast<const float4*>(p.part_o + sl * D) + i4);
+                            }
+                        }
+                        float Mn = Mr;
+#pragma unroll
+                        for (int u = 0; u < kFly; ++u)
+                            if (ml[u].y > 0.f) Mn = fmaxf(Mn, ml[u].x);
+                        const float a = (Mr == -INFINITY) ? 0.f : exp2f(Mr - Mn);
+                        acc.x *= a; acc.y *= a; acc.z *= a; acc.w *= a;
+                        Lr *= a;
+#pragma unroll
+                        for (int u = 0; u < kFly; ++u) {
+                            const float f = (ml[u].y > 0.f) ? exp2f(ml[u].x - Mn) : 0.f;
+                            acc.x = fmaf(f, v[u].x, acc.x);
+                            acc.y = fmaf(f, v[u].y, acc.y);
+                            acc.z = fmaf(f, v[u].z, acc.z);
+                            acc.w = fmaf(f, v[u].w, acc.w);
+                            Lr = fmaf(f, ml[u].y, Lr);
+                        }
+                        Mr = Mn;
+                    }
+                    const float L = Lr;
                     const bool live = L > 0.f;
                     const float inv = live ? 1.f / L : 0.f;
                     const int h = m / QL, jq = m - (m / QL) * QL;
-                    const float4 o = live ? make_float4(acc[k].x * inv, acc[k].y * inv, acc[k].z * inv, acc[k].w * inv)
+                    const float4 o = live ? make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv)
                                           : make_float4(0.f, 0.f, 0.f, 0.f);
                     if constexpr (CASC) {
                         // the pair's combined partial into its slot (items: part_offset)
@@ -1653,7 +1656,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                                           (sg.s < p.num_items ? p.part_offset : 0);
                         reinterpret_cast<float4*>(p.tmp_out + pi * D)[d >> 2] = o;
                         if (d == 0) {
-                            p.max_logits[pi] = live ? Mr[k] * kLn2 : -INFINITY;
+                            p.max_logits[pi] = live ? Mr * kLn2 : -INFINITY;
                             p.exp_sums[pi] = L;
                         }
                     } else {
@@ -1717,22 +1720,24 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
 
 template <typename T, int D, bool FUSED>
 cudaError_t dispatch_cc(const AttnParams& p, int gqa, const CUtensorMap& km, const CUtensorMap& vm, cudaStream_t st) {
+    // group sizes 1 and 2 (larger groups run the tensor-core math)
     switch (gqa) {
         case 1: return launch_math<CcMath<T, D, 1>, FUSED, false>(p, km, vm, st);
         case 2: return launch_math<CcMath<T, D, 2>, FUSED, false>(p, km, vm, st);
-        case 4: return launch_math<CcMath<T, D, 4>, FUSED, false>(p, km, vm, st);
-        case 8: return launch_math<CcMath<T, D, 8>, FUSED, false>(p, km, vm, st);
         default: return cudaErrorInvalidValue;
     }
 }
 
 // Math for the cache kind, head_dim, group size and q_len, then launch.  The
 // cascade pass takes the tensor-core math (an item has several query rows per
-// kv head; the sequences' own entries share its instantiation).
+// kv head; the sequences' own entries share its instantiation).  The choice is
+// attention_uses_tensor_cores(), the predicate the host also builds the tensor
+// maps from: the tensor-core maths issue 3-D tile copies (fp16/bf16) or
+// swizzled row copies (K8/V4) that only their own maps describe.
 template <bool FUSED, bool CASC>
 cudaError_t launch_attention_impl(const AttnParams& p, int cache_kind, int gqa, const CUtensorMap& km,
                                   const CUtensorMap& vm, cudaStream_t stream) {
-    if (CASC || p.q_len > 1 || cache_kind == PKV_CACHE_K8V4) {
+    if (attention_uses_tensor_cores(cache_kind, p.q_len, gqa, CASC)) {
         switch (cache_kind) {
             case PKV_CACHE_K8V4: {
                 const bool narrow = (p.num_heads / p.num_kv_heads) * p.q_len <= 8;

@@ -106,8 +106,11 @@ constexpr int kSegCost = 24;
 // Persistent attention kernel (attention.cu): one CTA per SM at most, the
 // (sequence, kv head, block) work list split into contiguous ranges.
 bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len);
-// Uses the CUDA-core math for fp16/bf16 with q_len 1, tensor cores otherwise.
-bool attention_uses_tensor_cores(int cache_kind, int q_len, bool cascade_pass = false);
+// Tensor-core maths for K8/V4, for cascade passes and whenever a kv head serves
+// at least kTcMinRows query rows (group size x q_len); the CUDA-core math for
+// fp16/bf16 below that (group size 1 or 2 decode).
+constexpr int kTcMinRows = 4;
+bool attention_uses_tensor_cores(int cache_kind, int q_len, int gqa, bool cascade_pass = false);
 // A pass of cascade attention: its own kernel instantiation (attention_cascade.cu)
 inline bool is_cascade_pass(const AttnParams& p) { return p.seq_start != nullptr || p.row_map != nullptr; }
 cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& k_map,
