@@ -1077,6 +1077,11 @@ struct Plan {
     int s0, ctx0, r0;
 };
 
+// Plan scratch: red[0 .. warps) holds the block-wide scan's per-warp totals (at
+// most 16 warps), red[16 .. 19) this CTA's resolved start / end.
+constexpr int kRedSlots = 24;
+constexpr int kRedU1 = 16, kRedU0 = 17, kRedStart0 = 18;
+
 struct SeqPos {
     int s, ctx;
     long long u, U, C;   // units, first unit, first cost position
@@ -1124,10 +1129,10 @@ __device__ __forceinline__ void plan_resolve(const AttnParams& p, const SeqPos& 
         flag[0] = sp.s;
         flag[2] = sp.ctx;
         flag[3] = sc > 0 ? int((sp.C - sp.U) / sc) : 0;
-        red[15] = sp.U;
-        red[14] = sp.U + max(0ll, X0 - sp.C - sc);
+        red[kRedStart0] = sp.U;
+        red[kRedU0] = sp.U + max(0ll, X0 - sp.C - sc);
     }
-    if (sp.C <= X1 && X1 < c_end) red[13] = sp.U + max(0ll, X1 - sp.C - sc);
+    if (sp.C <= X1 && X1 < c_end) red[kRedU1] = sp.U + max(0ll, X1 - sp.C - sc);
 }
 
 template <bool CASC>
@@ -1147,9 +1152,9 @@ __device__ void cta_plan(const AttnParams& p, int lane_idx, int nlanes, long lon
         flag[0] = B;         // s0
         flag[2] = 0;         // ctx0
         flag[3] = 0;         // r0
-        red[15] = 0;         // start0
-        red[14] = total_u;   // u0 (X0 past the end: empty range)
-        red[13] = total_u;   // u1
+        red[kRedStart0] = 0;   // start0
+        red[kRedU0] = total_u;   // u0 (X0 past the end: empty range)
+        red[kRedU1] = total_u;   // u1
     }
     __syncthreads();
     if (B <= nthr) {
@@ -1160,12 +1165,12 @@ __device__ void cta_plan(const AttnParams& p, int lane_idx, int nlanes, long lon
     }
     __syncthreads();
     pl.chunk = chunk;
-    pl.u0 = red[14];
-    pl.u1 = red[13];
+    pl.u0 = red[kRedU0];
+    pl.u1 = red[kRedU1];
     pl.s0 = flag[0];
     pl.ctx0 = flag[2];
     pl.r0 = flag[3];
-    pl.start0 = red[15];
+    pl.start0 = red[kRedStart0];
 }
 
 // ---------------------------------------------------------------- fused decode step: cache writes
@@ -1266,7 +1271,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     uint64_t* empty = full + S;
     int* poison = reinterpret_cast<int*>(empty + S);
     long long* red = reinterpret_cast<long long*>(smem + align_up(S * Math::STAGE + 16 * S + 4 * S, 16));
-    int* flag = reinterpret_cast<int*>(red + 16);
+    int* flag = reinterpret_cast<int*>(red + kRedSlots);
     float* mw = reinterpret_cast<float*>(flag + 4);                  // [NCW][16]
     float* lw = mw + NCW * kMaxRows;                                  // [NCW][16]
     float* rm = lw + NCW * kMaxRows;                                  // [16] merged row max
@@ -1673,7 +1678,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 template <class Math, bool FUSED>
 int smem_bytes(int stages, int M, int QL, int D) {
     constexpr int NCW = Math::NCW;
-    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + 16 * 8 + 16 + (2 * NCW + 2) * kMaxRows * 4 +
+    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + kRedSlots * 8 + 16 + (2 * NCW + 2) * kMaxRows * 4 +
            (FUSED && !checks_fit(M, QL, D) ? NCW * kCheckBytes : 0) + NCW * M * D * 4 + NCW * Math::SCRATCH + 1024 + 64;
 }
 
@@ -1740,6 +1745,8 @@ cudaError_t launch_attention_impl(const AttnParams& p, int cache_kind, int gqa, 
     if (attention_uses_tensor_cores(cache_kind, p.q_len, gqa, CASC)) {
         switch (cache_kind) {
             case PKV_CACHE_K8V4: {
+                if (!CASC && attention_tg_supported(cache_kind, p.head_dim, gqa, p.q_len, p.mode))
+                    return launch_attention_tg(p, gqa, km, vm, stream);
                 const bool narrow = (p.num_heads / p.num_kv_heads) * p.q_len <= 8;
                 if (p.head_dim == 128)
                     return narrow ? launch_math<TqMath<128, 1>, FUSED, CASC>(p, km, vm, stream)

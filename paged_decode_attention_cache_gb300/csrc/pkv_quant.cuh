@@ -23,17 +23,17 @@ struct QuantRow {
     __half vs, vz;    // V scale and zero of this lane's 32-dim group
 };
 
-// ksrc / vsrc point at this lane's E source values (fp16 or bf16 bits).
+// kb / vb: this lane's E source values (fp16 or bf16 bits).
 template <typename Src, int D>
-__device__ __forceinline__ QuantRow<D> quantize_row(const uint16_t* ksrc, const uint16_t* vsrc) {
+__device__ __forceinline__ QuantRow<D> quantize_vals(const uint16_t (&kb)[D / 32], const uint16_t (&vb)[D / 32]) {
     constexpr int E = D / 32;
     constexpr int LPG = 32 / E;   // lanes per 32-dim V group
     QuantRow<D> r;
     float k[E], v[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) {
-        k[e] = Half16<Src>::to_float(ksrc[e]);
-        v[e] = Half16<Src>::to_float(vsrc[e]);
+        k[e] = Half16<Src>::to_float(kb[e]);
+        v[e] = Half16<Src>::to_float(vb[e]);
     }
     // K: symmetric int8, one fp16 scale per (token, kv head)
     float a = 0.f;
@@ -72,6 +72,18 @@ __device__ __forceinline__ QuantRow<D> quantize_row(const uint16_t* ksrc, const 
         r.vpack |= uint32_t(c) << (4 * e);
     }
     return r;
+}
+
+// ksrc / vsrc point at this lane's E source values (fp16 or bf16 bits).
+template <typename Src, int D>
+__device__ __forceinline__ QuantRow<D> quantize_row(const uint16_t* ksrc, const uint16_t* vsrc) {
+    uint16_t kb[D / 32], vb[D / 32];
+#pragma unroll
+    for (int e = 0; e < D / 32; ++e) {
+        kb[e] = ksrc[e];
+        vb[e] = vsrc[e];
+    }
+    return quantize_vals<Src, D>(kb, vb);
 }
 
 }  // namespace pkv
