@@ -1745,8 +1745,6 @@ cudaError_t launch_attention_impl(const AttnParams& p, int cache_kind, int gqa, 
     if (attention_uses_tensor_cores(cache_kind, p.q_len, gqa, CASC)) {
         switch (cache_kind) {
             case PKV_CACHE_K8V4: {
-                if (!CASC && attention_tg_supported(cache_kind, p.head_dim, gqa, p.q_len, p.mode))
-                    return launch_attention_tg(p, gqa, km, vm, stream);
                 const bool narrow = (p.num_heads / p.num_kv_heads) * p.q_len <= 8;
                 if (p.head_dim == 128)
                     return narrow ? launch_math<TqMath<128, 1>, FUSED, CASC>(p, km, vm, stream)

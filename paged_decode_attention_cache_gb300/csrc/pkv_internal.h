@@ -111,11 +111,6 @@ bool attention_supported(int cache_kind, int head_dim, int gqa, int q_len);
 // fp16/bf16 below that (group size 1 or 2 decode).
 constexpr int kTcMinRows = 4;
 bool attention_uses_tensor_cores(int cache_kind, int q_len, int gqa, bool cascade_pass = false);
-// Balanced attention over a K8/V4 cache at head_dim 128 on the 5th-generation
-// tensor cores (attention_tg.cu): the launch when attention_tg_supported().
-bool attention_tg_supported(int cache_kind, int head_dim, int gqa, int q_len, int mode);
-cudaError_t launch_attention_tg(const AttnParams& p, int gqa, const CUtensorMap& k_map, const CUtensorMap& v_map,
-                                cudaStream_t stream);
 // A pass of cascade attention: its own kernel instantiation (attention_cascade.cu)
 inline bool is_cascade_pass(const AttnParams& p) { return p.seq_start != nullptr || p.row_map != nullptr; }
 cudaError_t launch_attention(AttnParams p, int cache_kind, int gqa, const CUtensorMap& k_map,
