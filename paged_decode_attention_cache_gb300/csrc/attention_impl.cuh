@@ -209,6 +209,7 @@ struct CcMath {
     // 11 consumer warps + the producer: 12 warps, three per SM sub-partition,
     // which leaves 168 registers a thread (this math runs group sizes 1 and 2)
     static constexpr int NCW = 11;
+    static constexpr int kSegCost = pkv::kSegCost;   // balanced: blocks' worth one more segment costs
     static constexpr int CH = D / 8;                               // 16-byte chunks per row
     static constexpr int LPT = (G * D / 64 > 8) ? G * D / 64 : 8;  // lanes per token (QK)
     static constexpr int TPP = 32 / LPT;                           // tokens per pass
@@ -420,6 +421,7 @@ struct TcMath {
     // 7 consumer warps + the producer: 8 warps, two per SM sub-partition, so a
     // thread may use up to 255 registers (the MMA fragments need ~230)
     static constexpr int NCW = 7;
+    static constexpr int kSegCost = pkv::kSegCost;
     static constexpr bool BF = KIND == PKV_CACHE_BF16;
     static constexpr int NKS = D / 16;
     static constexpr int NNT = D / 8;
@@ -651,6 +653,10 @@ struct TqMath {
     static constexpr int kD = D;
     // NT = 1: 11 consumer warps at <= 168 registers; NT = 2: 7 at <= 255
     static constexpr int NCW = NT == 1 ? 11 : 7;
+    // The K8/V4 math is bound by its consumers, so a segment switch (merge,
+    // piece, the next segment's queries) is not hidden behind the stream: it is
+    // charged more (32 measured best of 24, 32, 40, 48)
+    static constexpr int kSegCost = 32;
     static constexpr int NG = D / 32;      // V groups
     static constexpr int NKS = D / 16;     // k-steps of the score contraction
     static constexpr int KT = kBS * D;
@@ -738,16 +744,25 @@ struct TqMath {
             const int qr = n < M ? query_row<CASC>(p, s, j) : -1;
             const bool valid = qr >= 0;
             const size_t qoff = (size_t(valid ? qr : 0) * p.num_heads + kvh * G + h) * D;
+            // this thread's dims t*D/4 .. t*D/4 + D/4 - 1: D/2 contiguous bytes, as 16-byte loads
+            uint32_t qw[D / 8];
+            const uint4* qv = reinterpret_cast<const uint4*>(reinterpret_cast<const uint16_t*>(p.q) + qoff + t * (D / 4));
+#pragma unroll
+            for (int i = 0; i < D / 32; ++i) {
+                const uint4 x = valid ? qv[i] : make_uint4(0u, 0u, 0u, 0u);
+                qw[4 * i] = x.x; qw[4 * i + 1] = x.y; qw[4 * i + 2] = x.z; qw[4 * i + 3] = x.w;
+            }
+            if (p.q_dtype == PKV_BF16) {   // the MMA takes fp16: convert each pair
+#pragma unroll
+                for (int i = 0; i < D / 8; ++i) {
+                    const float2 f = Half16<__nv_bfloat16>::unpack2(qw[i]);
+                    qw[i] = pack2<false>(f.x, f.y);
+                }
+            }
 #pragma unroll
             for (int kk = 0; kk < NKS; ++kk) {
-                uint32_t lo = 0, hi = 0;
-                if (valid) {
-                    const int d0 = t * (D / 4) + 4 * kk;
-                    lo = pack2<false>(load_q(p.q, p.q_dtype, qoff + d0), load_q(p.q, p.q_dtype, qoff + d0 + 1));
-                    hi = pack2<false>(load_q(p.q, p.q_dtype, qoff + d0 + 2), load_q(p.q, p.q_dtype, qoff + d0 + 3));
-                }
-                qb[nt][kk][0] = lo;
-                qb[nt][kk][1] = hi;
+                qb[nt][kk][0] = qw[2 * kk];       // dims d0, d0 + 1 (d0 = t*D/4 + 4*kk)
+                qb[nt][kk][1] = qw[2 * kk + 1];   // dims d0 + 2, d0 + 3
             }
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
@@ -1698,6 +1713,7 @@ cudaError_t launch_math(AttnParams p, const CUtensorMap& km, const CUtensorMap& 
     stages = stages / Math::NCW * Math::NCW;   // every stage always belongs to the same consumer warp
     if (stages < Math::NCW) return cudaErrorInvalidConfiguration;
     p.stages = stages;
+    if (p.mode == kModeBalanced) p.seg_cost = Math::kSegCost;
     const int smem = smem_bytes<Math, FUSED>(stages, M, p.q_len, p.head_dim);
     static bool attr_set = false;
     if (!attr_set) {
