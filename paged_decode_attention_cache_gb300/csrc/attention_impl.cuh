@@ -210,6 +210,7 @@ struct CcMath {
     // which leaves 168 registers a thread (this math runs group sizes 1 and 2)
     static constexpr int NCW = 11;
     static constexpr int kSegCost = pkv::kSegCost;   // balanced: blocks' worth one more segment costs
+    static constexpr int kIssueGroup = 16;           // blocks the producer issues per pass
     static constexpr int CH = D / 8;                               // 16-byte chunks per row
     static constexpr int LPT = (G * D / 64 > 8) ? G * D / 64 : 8;  // lanes per token (QK)
     static constexpr int TPP = 32 / LPT;                           // tokens per pass
@@ -422,6 +423,10 @@ struct TcMath {
     // thread may use up to 255 registers (the MMA fragments need ~230)
     static constexpr int NCW = 7;
     static constexpr int kSegCost = pkv::kSegCost;
+    // Blocks the producer issues per pass: a pass waits on every stage it
+    // refills, so a smaller pass refills the first of them sooner (8 measured
+    // faster than 16 on the 32K and batch-8 decodes)
+    static constexpr int kIssueGroup = 8;
     static constexpr bool BF = KIND == PKV_CACHE_BF16;
     static constexpr int NKS = D / 16;
     static constexpr int NNT = D / 8;
@@ -657,6 +662,9 @@ struct TqMath {
     // piece, the next segment's queries) is not hidden behind the stream: it is
     // charged more (32 measured best of 24, 32, 40, 48)
     static constexpr int kSegCost = 32;
+    // 18 metadata copies and two tensor copies per block: 16 blocks per pass
+    // (8 and 32 measured slower)
+    static constexpr int kIssueGroup = 16;
     static constexpr int NG = D / 32;      // V groups
     static constexpr int NKS = D / 16;     // k-steps of the score contraction
     static constexpr int KT = kBS * D;
@@ -1354,7 +1362,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         // issues its own copies, so the per-block chain (wait, expect_tx, TMA)
         // of different blocks overlaps.  grp <= S: the previous use of every
         // stage touched in a pass was issued by an earlier pass.
-        const int grp = S < 16 ? S : 16;
+        const int grp = S < Math::kIssueGroup ? S : Math::kIssueGroup;
         int issued = 0;   // blocks issued by this CTA
         bool waited = false;
         Seg sg;
@@ -1598,16 +1606,16 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         if (piece) {
             // The last piece of a pair to finish combines all of them (no
             // waiting).  Publication: every thread's partial stores, the barrier,
-            // then one gpu-scope fence and the count by thread 0 (the barrier
-            // makes the other threads' stores part of what the fence releases).
+            // then the count by thread 0 with release semantics at gpu scope (the
+            // barrier makes the other threads' stores part of what it releases).
             named_barrier_sync(1, CT);
             const int c_lo = int((sg.pair_start + sg.cost_base - p.seg_cost) / chunk),
                       c_hi = int((sg.pair_start + sg.nu - 1 + sg.cost_base - p.seg_cost) / chunk);
             const int np = c_hi - c_lo + 1;
             if (tid == 0) {
-                __threadfence();
-                const int prev = atomicAdd(&p.counters[pair], 1);
-                __threadfence();   // acquire: the other pieces' partials before our loads
+                // release: this CTA's partial stores (ordered by the barrier);
+                // acquire: the other pieces' partials before our loads
+                const int prev = atomic_add_acq_rel_gpu(&p.counters[pair], 1);
                 flag[1] = (prev == np - 1) ? 1 : 0;
             }
             named_barrier_sync(1, CT);

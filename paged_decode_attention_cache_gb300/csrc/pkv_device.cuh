@@ -20,6 +20,18 @@ __device__ __forceinline__ void flag_error(uint32_t* err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }
 
+// atomicAdd at gpu scope with acquire-release semantics: the writes that
+// precede it (this thread's, and those ordered before it by a CTA barrier) are
+// visible to whoever observes the new count, and the writes released by earlier
+// adders are visible to this thread afterwards.  One operation instead of a
+// sequentially consistent fence on each side of a relaxed add (measured ~0.7 us
+// less per publication under a full DRAM stream).
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int* addr, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
