@@ -253,8 +253,10 @@ size_t pkv_balanced_workspace_bytes(int32_t num_seqs, int32_t num_kv_heads, int3
  * count decides who, nobody waits).
  *   workspace  device memory of pkv_balanced_workspace_bytes() bytes, 256-byte
  *              aligned, ZERO-FILLED before its first use; every call leaves its
- *              counters at zero again, so it can be reused without clearing
- *              (clear it again after a call that reported a device error).
+ *              counters at zero again, so it can be reused without clearing by
+ *              calls with the same num_seqs, num_kv_heads and head_dim (the
+ *              counters' offset depends on them; clear it before a call with
+ *              other sizes, and after a call that reported a device error).
  *              Calls that share one workspace must not overlap on the GPU.
  */
 pkv_status pkv_paged_attention_balanced(void *out, pkv_dtype out_dtype, const void *q, pkv_dtype q_dtype,
