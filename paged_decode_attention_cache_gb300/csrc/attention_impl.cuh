@@ -532,7 +532,8 @@ struct TcMath {
             bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
             const float mn = fmaxf(m_run[r], bm);
             const float mu = (mn == -INFINITY) ? 0.f : mn;
-            alpha[r] = exp2f(m_run[r] - mu);
+            // nothing accumulated yet (padding rows stay so): no rescale
+            alpha[r] = (m_run[r] == -INFINITY) ? 1.f : exp2f(m_run[r] - mu);
             float rs = 0.f;
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt)
@@ -662,9 +663,9 @@ struct TqMath {
     // piece, the next segment's queries) is not hidden behind the stream: it is
     // charged more (32 measured best of 24, 32, 40, 48)
     static constexpr int kSegCost = 32;
-    // 18 metadata copies and two tensor copies per block: 16 blocks per pass
-    // (8 and 32 measured slower)
-    static constexpr int kIssueGroup = 16;
+    // 18 metadata copies and two tensor copies per block: 22 blocks per pass,
+    // two per consumer warp (8, 11, 12, 16 and 32 measured slower)
+    static constexpr int kIssueGroup = 22;
     static constexpr int NG = D / 32;      // V groups
     static constexpr int NKS = D / 16;     // k-steps of the score contraction
     static constexpr int KT = kBS * D;
@@ -679,13 +680,15 @@ struct TqMath {
     static constexpr int STAGE = align_up(OFF_VZ + VS, 1024);
     static constexpr int SCRATCH = 0;
     static_assert(OFF_V % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1 KB alignment");
+    static_assert(OFF_VS % 16 == 0 && OFF_VZ % 16 == 0, "scale rows are read 16 bytes at a time");
 
     uint32_t qb[NT][NKS][2];   // Q^T operand: query column g (+8), this thread's dims
     float o[NT][2 * NG][4];    // O^T accumulators: M tile (group, i) x 8 query columns
     float cz[NT][4];           // Z^T P^T: rows = groups
     float m_run[NT][2], l_part[NT][2];   // per query column 2t, 2t+1 (l: this thread's tokens)
     int lim[NT][2];
-    int lo_;   // first visible token (sliding window)
+    int lo_;       // first visible token (sliding window)
+    int lim_lo_;   // smallest lim over this thread's live columns (no live column: INT_MAX)
     float scale_log2_;
 
     static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
@@ -785,6 +788,12 @@ struct TqMath {
             for (int mt = 0; mt < 2 * NG; ++mt) o[nt][mt][0] = o[nt][mt][1] = o[nt][mt][2] = o[nt][mt][3] = 0.f;
             cz[nt][0] = cz[nt][1] = cz[nt][2] = cz[nt][3] = 0.f;
         }
+        lim_lo_ = INT_MAX;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e)
+                if (lim[nt][e] > 0) lim_lo_ = min(lim_lo_, lim[nt][e]);
     }
 
     __device__ __forceinline__ void block(const uint8_t* stg, int pos0, int ntok, uint8_t*, int lane) {
@@ -817,12 +826,24 @@ struct TqMath {
         const __half* ksh = reinterpret_cast<const __half*>(stg + OFF_KS);
         const float k0 = __half2float(ksh[g]) * scale_log2_, k1 = __half2float(ksh[g + 8]) * scale_log2_;
         const int pg = pos0 + g, pg8 = pos0 + g + 8;
+        if (pos0 >= lo_ && pos0 + kBS <= lim_lo_) {
+            // the whole block is visible to every live column of this thread;
+            // columns with nothing visible (padding) stay masked
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-            sc[nt][0] = (pg < lim[nt][0] && pg >= lo_) ? sc[nt][0] * k0 : -INFINITY;
-            sc[nt][1] = (pg < lim[nt][1] && pg >= lo_) ? sc[nt][1] * k0 : -INFINITY;
-            sc[nt][2] = (pg8 < lim[nt][0] && pg8 >= lo_) ? sc[nt][2] * k1 : -INFINITY;
-            sc[nt][3] = (pg8 < lim[nt][1] && pg8 >= lo_) ? sc[nt][3] * k1 : -INFINITY;
+            for (int nt = 0; nt < NT; ++nt) {
+                sc[nt][0] = lim[nt][0] > 0 ? sc[nt][0] * k0 : -INFINITY;
+                sc[nt][1] = lim[nt][1] > 0 ? sc[nt][1] * k0 : -INFINITY;
+                sc[nt][2] = lim[nt][0] > 0 ? sc[nt][2] * k1 : -INFINITY;
+                sc[nt][3] = lim[nt][1] > 0 ? sc[nt][3] * k1 : -INFINITY;
+            }
+        } else {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                sc[nt][0] = (pg < lim[nt][0] && pg >= lo_) ? sc[nt][0] * k0 : -INFINITY;
+                sc[nt][1] = (pg < lim[nt][1] && pg >= lo_) ? sc[nt][1] * k0 : -INFINITY;
+                sc[nt][2] = (pg8 < lim[nt][0] && pg8 >= lo_) ? sc[nt][2] * k1 : -INFINITY;
+                sc[nt][3] = (pg8 < lim[nt][1] && pg8 >= lo_) ? sc[nt][3] * k1 : -INFINITY;
+            }
         }
         // ------------------------------------------------ online softmax per query column
         float alpha[NT][2];
@@ -837,7 +858,8 @@ struct TqMath {
                 bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
                 const float mn = fmaxf(m_run[nt][e], bm);
                 const float mu = (mn == -INFINITY) ? 0.f : mn;
-                alpha[nt][e] = exp2f(m_run[nt][e] - mu);
+                // nothing accumulated yet (padding columns stay so): no rescale
+                alpha[nt][e] = (m_run[nt][e] == -INFINITY) ? 1.f : exp2f(m_run[nt][e] - mu);
                 const float p0 = exp2f(sc[nt][e] - mu), p1 = exp2f(sc[nt][2 + e] - mu);
                 sc[nt][e] = p0;
                 sc[nt][2 + e] = p1;
@@ -868,19 +890,37 @@ struct TqMath {
         // rows past the context hold NaN and are zeroed (their P is 0)
         constexpr int RW = (NG * 2 + 3) / 4;   // 32-bit words per token row
         uint32_t sr[4][RW], zr[4][RW];
+        if constexpr (RW == 2) {
+            // tokens (2t, 2t+1) and (2t+8, 2t+9): 16 contiguous bytes each
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int tk = 2 * t + (i & 1) + 8 * (i >> 1);
-            const uint32_t* sp = reinterpret_cast<const uint32_t*>(stg + OFF_VS + tk * NG * 2);
-            const uint32_t* zp = reinterpret_cast<const uint32_t*>(stg + OFF_VZ + tk * NG * 2);
-#pragma unroll
-            for (int q = 0; q < RW; ++q) {
-                sr[i][q] = sp[q];
-                zr[i][q] = zp[q];
+            for (int h = 0; h < 2; ++h) {
+                const int tk = 2 * t + 8 * h;
+                const uint4 sv = *reinterpret_cast<const uint4*>(stg + OFF_VS + tk * NG * 2);
+                const uint4 zv = *reinterpret_cast<const uint4*>(stg + OFF_VZ + tk * NG * 2);
+                sr[2 * h][0] = sv.x; sr[2 * h][1] = sv.y; sr[2 * h + 1][0] = sv.z; sr[2 * h + 1][1] = sv.w;
+                zr[2 * h][0] = zv.x; zr[2 * h][1] = zv.y; zr[2 * h + 1][0] = zv.z; zr[2 * h + 1][1] = zv.w;
             }
-            if (tk >= ntok) {
+        } else {
 #pragma unroll
-                for (int q = 0; q < RW; ++q) sr[i][q] = zr[i][q] = 0u;
+            for (int i = 0; i < 4; ++i) {
+                const int tk = 2 * t + (i & 1) + 8 * (i >> 1);
+                const uint32_t* sp = reinterpret_cast<const uint32_t*>(stg + OFF_VS + tk * NG * 2);
+                const uint32_t* zp = reinterpret_cast<const uint32_t*>(stg + OFF_VZ + tk * NG * 2);
+#pragma unroll
+                for (int q = 0; q < RW; ++q) {
+                    sr[i][q] = sp[q];
+                    zr[i][q] = zp[q];
+                }
+            }
+        }
+        if (ntok < kBS) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int tk = 2 * t + (i & 1) + 8 * (i >> 1);
+                if (tk >= ntok) {
+#pragma unroll
+                    for (int q = 0; q < RW; ++q) sr[i][q] = zr[i][q] = 0u;
+                }
             }
         }
         // ------------------------------------------------ O^T += V^T (P^T * s), Z^T P^T
@@ -1475,10 +1515,13 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 cp_async_commit();
             }
         }
-        for (int i = (warp - jbase % NCW + NCW) % NCW; i < n; i += NCW) {
-            const int j = jbase + i;
-            const int st = j % S;
-            const bool ok = mbar_wait(&full[st], uint32_t((j / S) & 1));
+        const int i_first = (warp - jbase % NCW + NCW) % NCW;
+        // stage and phase of this warp's blocks, advanced by NCW per block (S is
+        // a multiple of NCW) instead of a division per block
+        int st = (jbase + i_first) % S;
+        uint32_t phase = uint32_t((jbase + i_first) / S) & 1u;
+        for (int i = i_first; i < n; i += NCW) {
+            const bool ok = mbar_wait(&full[st], phase);
             if (!ok && lane == 0) flag_error(p.err, PKV_DEVERR_TIMEOUT);
             const int b = sg.b0 + i;
             int ntok = (b == sg.nb - 1) ? sg.ctx - b * kBS : kBS;
@@ -1508,6 +1551,11 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             if (FUSED && patched) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[st]);
+            st += NCW;
+            if (st >= S) {
+                st -= S;
+                phase ^= 1u;
+            }
         }
         jbase += n;
         mth.finish(lane);
