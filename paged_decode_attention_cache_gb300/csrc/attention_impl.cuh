@@ -162,6 +162,23 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+// The same four codes kept biased: fp16x2 of the exact integers c + 1152 (two
+// byte permutes and no subtraction); the caller takes 1152 * sum(q) off each
+// score instead.
+__device__ __forceinline__ void s8x4_to_f16x4_biased(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    const uint32_t x = w ^ 0x80808080u;
+    lo = __byte_perm(x, 0x64646464u, 0x5140);
+    hi = __byte_perm(x, 0x64646464u, 0x7362);
+}
+
+// 2^x by the hardware's approximate exponential with subnormal results
+// flushed to zero (a weight below 2^-126 of the row maximum)
+__device__ __forceinline__ float exp2_ftz(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Nibble i of both 16-bit halves of w -> fp16x2 of the exact integers 0..15.
 __device__ __forceinline__ uint32_t u4pair_to_f16x2(uint32_t w, int i) {
     const uint32_t x = ((w >> (4 * i)) & 0x000F000Fu) | 0x64006400u;   // 1024 + code
@@ -687,6 +704,7 @@ struct TqMath {
     float cz[NT][4];           // Z^T P^T: rows = groups
     float m_run[NT][2], l_part[NT][2];   // per query column 2t, 2t+1 (l: this thread's tokens)
     int lim[NT][2];
+    float kbias[NT][2];   // 1152 * sum of q over the head dims, query columns 2t, 2t+1
     int lo_;       // first visible token (sliding window)
     int lim_lo_;   // smallest lim over this thread's live columns (no live column: INT_MAX)
     float scale_log2_;
@@ -770,11 +788,19 @@ struct TqMath {
                     qw[i] = pack2<false>(f.x, f.y);
                 }
             }
+            float qs = 0.f;   // this thread's share of column g's sum of q (in fp16, as the MMA sees it)
 #pragma unroll
             for (int kk = 0; kk < NKS; ++kk) {
                 qb[nt][kk][0] = qw[2 * kk];       // dims d0, d0 + 1 (d0 = t*D/4 + 4*kk)
                 qb[nt][kk][1] = qw[2 * kk + 1];   // dims d0 + 2, d0 + 3
+                const float2 f0 = Half16<__half>::unpack2(qw[2 * kk]), f1 = Half16<__half>::unpack2(qw[2 * kk + 1]);
+                qs += (f0.x + f0.y) + (f1.x + f1.y);
             }
+            qs += __shfl_xor_sync(0xffffffffu, qs, 1);
+            qs += __shfl_xor_sync(0xffffffffu, qs, 2);
+            // column 2t + e's sum sits in the lanes of g = 2t + e
+            kbias[nt][0] = 1152.f * __shfl_sync(0xffffffffu, qs, (2 * t) * 4);
+            kbias[nt][1] = 1152.f * __shfl_sync(0xffffffffu, qs, (2 * t + 1) * 4);
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int n2 = 8 * nt + 2 * t + e;
@@ -817,10 +843,18 @@ struct TqMath {
 #pragma unroll
         for (int kk = 0; kk < NKS; ++kk) {
             uint32_t a[4];
-            s8x4_to_f16x4(w[0][kk], a[0], a[2]);
-            s8x4_to_f16x4(w[1][kk], a[1], a[3]);
+            s8x4_to_f16x4_biased(w[0][kk], a[0], a[2]);
+            s8x4_to_f16x4_biased(w[1][kk], a[1], a[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_f16(sc[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
+        // take the codes' bias off: S = sum (c + 1152) q - 1152 sum q
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            sc[nt][0] -= kbias[nt][0];
+            sc[nt][1] -= kbias[nt][1];
+            sc[nt][2] -= kbias[nt][0];
+            sc[nt][3] -= kbias[nt][1];
         }
         // K scale per token, base-2 softmax scale, causal / context mask
         const __half* ksh = reinterpret_cast<const __half*>(stg + OFF_KS);
@@ -859,8 +893,8 @@ struct TqMath {
                 const float mn = fmaxf(m_run[nt][e], bm);
                 const float mu = (mn == -INFINITY) ? 0.f : mn;
                 // nothing accumulated yet (padding columns stay so): no rescale
-                alpha[nt][e] = (m_run[nt][e] == -INFINITY) ? 1.f : exp2f(m_run[nt][e] - mu);
-                const float p0 = exp2f(sc[nt][e] - mu), p1 = exp2f(sc[nt][2 + e] - mu);
+                alpha[nt][e] = (m_run[nt][e] == -INFINITY) ? 1.f : exp2_ftz(m_run[nt][e] - mu);
+                const float p0 = exp2_ftz(sc[nt][e] - mu), p1 = exp2_ftz(sc[nt][2 + e] - mu);
                 sc[nt][e] = p0;
                 sc[nt][2 + e] = p1;
                 l_part[nt][e] = l_part[nt][e] * alpha[nt][e] + (p0 + p1);
