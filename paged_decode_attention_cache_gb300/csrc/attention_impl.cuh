@@ -1371,11 +1371,9 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     int* flag = reinterpret_cast<int*>(red + kRedSlots);
     float* mw = reinterpret_cast<float*>(flag + 4);                  // [NCW][16]
     float* lw = mw + NCW * kMaxRows;                                  // [NCW][16]
-    float* rm = lw + NCW * kMaxRows;                                  // [16] merged row max
-    float* rl = rm + kMaxRows;                                        // [16] merged row sum
     // fused step, g = 1 only: [NCW][16 int64 + 16 int32] slot checks (otherwise
     // they sit in the merge buffer behind the staged rows)
-    uint8_t* ck = reinterpret_cast<uint8_t*>(rl + kMaxRows);
+    uint8_t* ck = reinterpret_cast<uint8_t*>(lw + NCW * kMaxRows);
     const bool own_ck = FUSED && !checks_fit(M, QL, D);
     float* ob = reinterpret_cast<float*>(ck + (own_ck ? kCheckBytes * NCW : 0));   // [NCW][M][D], ob_idx order
     uint8_t* scratch = reinterpret_cast<uint8_t*>(ob + size_t(NCW) * M * D);   // [NCW][SCRATCH]
@@ -1597,37 +1595,31 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         // ------------------------------------------------ merge the warps' states for this segment
         mth.store(ob + size_t(warp) * M * D, mw + warp * kMaxRows, lw + warp * kMaxRows, M, lane);
         named_barrier_sync(1, CT);
-        // per row: the segment max, each warp's weight 2^(m_w - max) (written over m_w) and the sum
-        if (tid < M) {
-            float Mx = -INFINITY;
-#pragma unroll
-            for (int w2 = 0; w2 < NCW; ++w2) Mx = fmaxf(Mx, mw[w2 * kMaxRows + tid]);
-            float L = 0.f;
-#pragma unroll
-            for (int w2 = 0; w2 < NCW; ++w2) {
-                const float mm = mw[w2 * kMaxRows + tid];
-                const float f = (mm == -INFINITY) ? 0.f : exp2f(mm - Mx);
-                mw[w2 * kMaxRows + tid] = f;
-                L = fmaf(lw[w2 * kMaxRows + tid], f, L);
-            }
-            rm[tid] = Mx;
-            rl[tid] = L;
-        }
-        named_barrier_sync(1, CT);
         // Every shared-memory read of the merge comes before the first global
         // store: a store can wait behind this SM's queue of TMA reads, and a
-        // later shared load issued behind it would wait as long.
+        // later shared load issued behind it would wait as long.  Each thread
+        // works out its row's segment max, the warps' weights 2^(m_w - max) and
+        // the sum itself (no second barrier).
         const int n4 = (M * D) >> 2;
         float4 res[kPer];
+        float resM[kPer], resL[kPer];
 #pragma unroll
         for (int k = 0; k < kPer; ++k) {
             const int i4 = tid + k * CT;
             float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
+            float Mx = -INFINITY, L = 0.f;
             if (i4 < n4) {
                 const int m = (i4 << 2) / D, d = (i4 << 2) - m * D;
+                float mwv[NCW];
 #pragma unroll
                 for (int w2 = 0; w2 < NCW; ++w2) {
-                    const float f = mw[w2 * kMaxRows + m];
+                    mwv[w2] = mw[w2 * kMaxRows + m];
+                    Mx = fmaxf(Mx, mwv[w2]);
+                }
+#pragma unroll
+                for (int w2 = 0; w2 < NCW; ++w2) {
+                    const float f = (mwv[w2] == -INFINITY) ? 0.f : exp2f(mwv[w2] - Mx);
+                    L = fmaf(lw[w2 * kMaxRows + m], f, L);
                     const float4 v = *reinterpret_cast<const float4*>(ob + size_t(w2) * M * D + ob_idx(m, d, D));
                     O.x = fmaf(v.x, f, O.x);
                     O.y = fmaf(v.y, f, O.y);
@@ -1636,14 +1628,8 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 }
             }
             res[k] = O;
-        }
-        float resM[kPer], resL[kPer];
-#pragma unroll
-        for (int k = 0; k < kPer; ++k) {
-            const int i4 = tid + k * CT;
-            const int m = i4 < n4 ? (i4 << 2) / D : 0;
-            resM[k] = rm[m];
-            resL[k] = rl[m];
+            resM[k] = Mx;
+            resL[k] = L;
         }
         const int pair = sg.s * Hkv + sg.kvh;
         const bool piece = (p.mode == kModeBalanced) && !sg.whole;
@@ -1783,7 +1769,7 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
 template <class Math, bool FUSED>
 int smem_bytes(int stages, int M, int QL, int D) {
     constexpr int NCW = Math::NCW;
-    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + kRedSlots * 8 + 16 + (2 * NCW + 2) * kMaxRows * 4 +
+    return stages * Math::STAGE + 16 * stages + 4 * stages + 16 + kRedSlots * 8 + 16 + 2 * NCW * kMaxRows * 4 +
            (FUSED && !checks_fit(M, QL, D) ? NCW * kCheckBytes : 0) + NCW * M * D * 4 + NCW * Math::SCRATCH + 1024 + 64;
 }
 
