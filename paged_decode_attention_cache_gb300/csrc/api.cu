@@ -176,6 +176,12 @@ pkv_status cache_maps(const pkv_cache* c, CUtensorMap* km, CUtensorMap* vm, bool
     return tile_map(vm, c->v, rows, int64_t(H) * D * 2, D * 2, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
+#ifdef PKV_TIMELINE
+// Timeline build only: the device buffer the attention kernels stamp (see
+// attention_impl.cuh); set by pkv_timeline_attach, read by every later call.
+unsigned long long* g_timeline = nullptr;
+#endif
+
 // Shared checks + parameter block of both attention entry points.
 pkv_status attn_setup(pkv::AttnParams* p, const void* q, pkv_dtype q_dtype, int32_t num_heads, float scale,
                       const pkv_cache* cache, const pkv_seqs* seqs, uint32_t* err, int* gqa) {
@@ -197,6 +203,9 @@ pkv_status attn_setup(pkv::AttnParams* p, const void* q, pkv_dtype q_dtype, int3
         return fail(PKV_ERR_UNSUPPORTED, "no kernel for cache kind %d, head_dim %d, group %d, q_len %d", cache->kind,
                     cache->head_dim, *gqa, seqs->q_len);
     *p = pkv::AttnParams{};
+#ifdef PKV_TIMELINE
+    p->timeline = g_timeline;
+#endif
     p->q = q;
     p->q_dtype = q_dtype;
     p->scale_log2 = scale * 1.4426950408889634f;
@@ -229,6 +238,12 @@ pkv_status attn_launch(pkv::AttnParams p, const pkv_cache* cache, int gqa, pkv_s
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 }  // namespace
+
+#ifdef PKV_TIMELINE
+extern "C" void pkv_timeline_attach(void* device_buffer) {
+    g_timeline = static_cast<unsigned long long*>(device_buffer);
+}
+#endif
 
 extern "C" {
 

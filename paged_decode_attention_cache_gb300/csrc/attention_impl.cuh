@@ -1178,6 +1178,31 @@ struct Plan {
 // most 16 warps), red[16 .. 19) this CTA's resolved start / end.
 constexpr int kRedSlots = 24;
 constexpr int kRedU1 = 16, kRedU0 = 17, kRedStart0 = 18;
+constexpr int kRedTl = 20;   // timeline build: this launch's index
+
+// Timeline build (-DPKV_TIMELINE, a separate library that the product never
+// loads): thread 0 / lane 0 stamp %globaltimer at fixed points of each CTA's
+// run into p.timeline: word 0 counts CTA entries (launch index = count / grid),
+// then [launch % kTlLaunches][CTA][kTlWords]: 0 entry, 1 plan done, 2 first
+// copies issued (after the grid dependency wait), 3 first block in shared
+// memory, 4 + 4k + {0, 1, 2, 3} segment k (< kTlSegs): start, blocks merged,
+// piece published, end; 28 segments | combiner bits << 8 | piece bits << 16;
+// 29 + k/4: blocks of segment k, 16 bits each.
+constexpr int kTlLaunches = 64, kTlCtas = 160, kTlWords = 32, kTlSegs = 6;
+#ifdef PKV_TIMELINE
+#define PKV_TL_AT(word, value)                                                                              \
+    do {                                                                                                    \
+        if (p.timeline && blockIdx.x < kTlCtas)                                                             \
+            p.timeline[1 + (size_t(tl_launch % kTlLaunches) * kTlCtas + blockIdx.x) * kTlWords + (word)] = \
+                (value);                                                                                    \
+    } while (0)
+#define PKV_TL(word) PKV_TL_AT(word, global_timer_ns())
+#else
+#define PKV_TL_AT(word, value) \
+    do {                       \
+    } while (0)
+#define PKV_TL(word) PKV_TL_AT(word, 0)
+#endif
 
 struct SeqPos {
     int s, ctx;
@@ -1388,6 +1413,17 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         }
         fence_barrier_init();
     }
+#ifdef PKV_TIMELINE
+    unsigned int tl_launch = 0;
+    if (tid == 0) {
+        tl_launch = p.timeline ? unsigned(atomicAdd(p.timeline, 1ull) / gridDim.x) : 0u;
+        red[kRedTl] = tl_launch;
+        PKV_TL(0);
+    }
+    int tl_seg = 0;
+    unsigned long long tl_flags = 0, tl_blocks = 0;
+    bool tl_first = true;
+#endif
 
     // ---- this CTA's range of units.  Split / balanced: the grid is Hkv lanes of
     // L CTAs; CTA c serves kv head c % Hkv over range c / Hkv of the lane's list,
@@ -1414,6 +1450,10 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     // launch's inputs (context lengths), which no kernel of this library writes; what follows
     // waits for the previous kernel of the stream before it reads the cache or
     // writes anything.
+#ifdef PKV_TIMELINE
+    tl_launch = unsigned(red[kRedTl]);   // the plan's barriers made it visible
+    if (tid == 0) PKV_TL(1);
+#endif
     if (tid == 0) grid_dep_launch();
 
     SegIter<CASC> it;
@@ -1448,6 +1488,9 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                     if (!waited) {
                         grid_dep_wait();
                         waited = true;
+#ifdef PKV_TIMELINE
+                        if (lane == 0) PKV_TL(2);
+#endif
                     }
                     const int j = issued + lane;
                     const int st = j % S;
@@ -1507,6 +1550,9 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
     Seg sg;
     while (it.next(p, sg)) {
         const int n = sg.b1 - sg.b0;
+#ifdef PKV_TIMELINE
+        if (tid == 0 && tl_seg < kTlSegs) PKV_TL(4 + 4 * tl_seg);
+#endif
         mth.template begin<CASC>(p, sg.s, sg.kvh, sg.ctx, lane);
         // Fused step: the warp that will consume a block holding new positions
         // [ctx - q_len, ctx) prefetches those rows from k_new / v_new into its
@@ -1554,6 +1600,10 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         uint32_t phase = uint32_t((jbase + i_first) / S) & 1u;
         for (int i = i_first; i < n; i += NCW) {
             const bool ok = mbar_wait(&full[st], phase);
+#ifdef PKV_TIMELINE
+            if (tl_first && warp == 0 && lane == 0) PKV_TL(3);
+            tl_first = false;
+#endif
             if (!ok && lane == 0) flag_error(p.err, PKV_DEVERR_TIMEOUT);
             const int b = sg.b0 + i;
             int ntok = (b == sg.nb - 1) ? sg.ctx - b * kBS : kBS;
@@ -1595,6 +1645,9 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
         // ------------------------------------------------ merge the warps' states for this segment
         mth.store(ob + size_t(warp) * M * D, mw + warp * kMaxRows, lw + warp * kMaxRows, M, lane);
         named_barrier_sync(1, CT);
+#ifdef PKV_TIMELINE
+        if (tid == 0 && tl_seg < kTlSegs) PKV_TL(4 + 4 * tl_seg + 1);
+#endif
         // Every shared-memory read of the merge comes before the first global
         // store: a store can wait behind this SM's queue of TMA reads, and a
         // later shared load issued behind it would wait as long.  Each thread
@@ -1687,6 +1740,12 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                 flag[1] = (prev == np - 1) ? 1 : 0;
             }
             named_barrier_sync(1, CT);
+#ifdef PKV_TIMELINE
+            if (tid == 0 && tl_seg < kTlSegs) {
+                PKV_TL(4 + 4 * tl_seg + 2);
+                tl_flags |= (1ull << (16 + tl_seg)) | (flag[1] ? (1ull << (8 + tl_seg)) : 0ull);
+            }
+#endif
             if (flag[1]) {
                 // Pieces hold unnormalised sums relative to their own max m_c:
                 // O = sum_c 2^(m_c - M) O_c, L = sum_c 2^(m_c - M) l_c.  The pieces'
@@ -1763,6 +1822,17 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
             }
         }
         named_barrier_sync(1, CT);   // the merge buffers are reused by the next segment
+#ifdef PKV_TIMELINE
+        if (tid == 0) {
+            if (tl_seg < kTlSegs) {
+                PKV_TL(4 + 4 * tl_seg + 3);
+                if (tl_seg < 4) tl_blocks |= (unsigned long long)(n & 0xffff) << (16 * tl_seg);
+            }
+            ++tl_seg;
+            PKV_TL_AT(28, tl_flags | (unsigned long long)(tl_seg < 255 ? tl_seg : 255));
+            PKV_TL_AT(29, tl_blocks);
+        }
+#endif
     }
 }
 

@@ -87,6 +87,9 @@ struct AttnParams {
     // 1: block_tables / context_lens come from the previous kernel (the sparse
     // set-up), so the kernel waits for it before planning
     int32_t wait_first;
+    // timeline build only (PKV_TIMELINE): per-CTA %globaltimer stamps, see
+    // attention_impl.cuh; null otherwise
+    unsigned long long* timeline;
     float* part_o;      // balanced workspace: [slots, 16, head_dim] unnormalised partial outputs
     float* part_ml;     // [slots, 16, 2] (max, sum) in base-2 units
     int32_t* counters;  // [num_seqs * num_kv_heads] pieces finished per (sequence, kv head)

@@ -50,15 +50,27 @@ _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 
 
+_lib_path: Optional[str] = None   # None: libpkv.so (build.LIB)
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _lib_path or _build.LIB
+
+
+def select_library(path: str) -> None:
+    """Load another build of the same library (the timeline build) instead of
+    libpkv.so; only before the first call."""
+    global _lib_path
+    if _lib is not None and path != library_path():
+        raise RuntimeError("the library is already loaded")
+    _lib_path = path
 
 
 def lib():
     """Load libpkv.so; raises if it has not been built."""
     global _lib
     if _lib is None:
-        path = _build.LIB
+        path = library_path()
         if not os.path.exists(path):
             raise RuntimeError(f"{path} is not built: call __graft_entry__.build() (nvcc, sm_103a)")
         L = ctypes.CDLL(path)
