@@ -151,10 +151,32 @@ namespace {
 //     meant.
 constexpr int kSetupThreads = 1024;
 
+// Whether member k of its item shares the item's prefix blocks (one warp).
+__device__ __forceinline__ bool cascade_member_ok(const CascadeParams& p, int k, int lane) {
+    const int item = k / p.width;
+    const int s = p.members[k], s0 = p.members[size_t(item) * p.width], nb = p.item_blocks[item];
+    bool ok = s0 >= 0 && s0 < p.num_seqs && nb > 0 && nb <= p.max_blocks && s >= 0 && s < p.num_seqs &&
+              p.context_lens[s] >= nb * kBlockSize;
+    if (ok) {
+        const int32_t* a = p.block_tables + size_t(s) * p.max_blocks;
+        const int32_t* b = p.block_tables + size_t(s0) * p.max_blocks;
+        bool same = true;
+        for (int x = lane; x < nb; x += 32) same &= (a[x] == b[x]);
+        ok = __all_sync(0xffffffffu, same);
+    }
+    return ok;
+}
+
+// Its inputs (members, item blocks, block tables, context lengths) are the
+// caller's: each warp checks its first member against its item's prefix before
+// the grid dependency wait, under the previous kernel's tail; every global
+// write comes after it.
 __global__ void __launch_bounds__(kSetupThreads) cascade_setup_kernel(CascadeParams p) {
-    grid_dep_wait();
-    grid_dep_launch();
+    grid_dep_launch();   // the attention waits for this grid to complete anyway
     const int ni = p.num_items, W = p.width, tid = threadIdx.x;
+    const int warp0 = tid >> 5, lane0 = tid & 31;
+    const bool ok_first = warp0 < ni * W ? cascade_member_ok(p, warp0, lane0) : false;
+    grid_dep_wait();
     for (int i = tid; i < p.num_counters; i += kSetupThreads) p.counters[i] = 0;
     for (int s = tid; s < p.num_seqs; s += kSetupThreads) {
         const int e = ni + s;
@@ -176,15 +198,7 @@ __global__ void __launch_bounds__(kSetupThreads) cascade_setup_kernel(CascadePar
     for (int k = warp; k < ni * W; k += kSetupThreads / 32) {
         const int item = k / W;
         const int s = p.members[k], s0 = p.members[size_t(item) * W], nb = p.item_blocks[item];
-        bool ok = s0 >= 0 && s0 < p.num_seqs && nb > 0 && nb <= p.max_blocks && s >= 0 && s < p.num_seqs &&
-                  p.context_lens[s] >= nb * kBlockSize;
-        if (ok) {
-            const int32_t* a = p.block_tables + size_t(s) * p.max_blocks;
-            const int32_t* b = p.block_tables + size_t(s0) * p.max_blocks;
-            bool same = true;
-            for (int x = lane; x < nb; x += 32) same &= (a[x] == b[x]);
-            ok = __all_sync(0xffffffffu, same);
-        }
+        const bool ok = k == warp ? ok_first : cascade_member_ok(p, k, lane);
         int row = -1;
         if (lane == 0) {
             // one item per sequence: the first to claim it
@@ -208,20 +222,20 @@ __global__ void __launch_bounds__(kSetupThreads) cascade_setup_kernel(CascadePar
 constexpr int kSparseThreads = 1024;
 constexpr int kSparseWarps = kSparseThreads / 32;
 
+// Its inputs (lists, counts, block tables, context lengths) are the caller's,
+// which no kernel of the library writes: they are read, and the first round's
+// kept pages and block ids worked out, before the grid dependency wait, under
+// the previous kernel's tail; every global write comes after it.
 __global__ void __launch_bounds__(kSparseThreads) sparse_setup_kernel(SparseParams p) {
-    grid_dep_wait();
-    grid_dep_launch();
+    grid_dep_launch();   // the attention waits for this grid to complete anyway
     __shared__ int w_max[kSparseWarps], w_cnt[kSparseWarps];
     __shared__ int any_bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, s = blockIdx.x;
-    for (int i = s * kSparseThreads + tid; i < p.num_counters; i += gridDim.x * kSparseThreads) p.counters[i] = 0;
     if (tid == 0) any_bad = 0;
     int ctx = p.context_lens[s];
     if (ctx < 0) ctx = 0;
-    if (ctx > p.max_blocks * kBlockSize) {
-        ctx = p.max_blocks * kBlockSize;
-        if (tid == 0) flag_error(p.err, PKV_DEVERR_CAPACITY);
-    }
+    const bool capped = ctx > p.max_blocks * kBlockSize;
+    if (capped) ctx = p.max_blocks * kBlockSize;
     const int npages = (ctx + kBlockSize - 1) / kBlockSize;
     int cnt = p.page_counts[s];
     cnt = cnt < 0 ? 0 : (cnt > p.max_pages ? p.max_pages : cnt);
@@ -233,6 +247,7 @@ __global__ void __launch_bounds__(kSparseThreads) sparse_setup_kernel(SparsePara
         const int i = base + tid;
         const int pg = i < cnt ? list[i] : -1;
         const bool in_range = i < cnt && pg >= 0 && pg < npages;
+        const int32_t blk = in_range ? bt[pg] : 0;   // an input: fetched ahead of the wait
         // inclusive prefix max of in-range pages within the warp
         int incl = in_range ? pg : -1;
 #pragma unroll
@@ -253,14 +268,24 @@ __global__ void __launch_bounds__(kSparseThreads) sparse_setup_kernel(SparsePara
         __syncthreads();
         int pos = n + __popc(m & ((1u << lane) - 1u));
         for (int w2 = 0; w2 < warp; ++w2) pos += w_cnt[w2];
-        if (keep) out[pos] = bt[pg];
+        if (base == 0) {   // the first global write: the previous kernel must be done
+            grid_dep_wait();
+            for (int c = s * kSparseThreads + tid; c < p.num_counters; c += gridDim.x * kSparseThreads)
+                p.counters[c] = 0;
+        }
+        if (keep) out[pos] = blk;
         for (int w2 = 0; w2 < kSparseWarps; ++w2) {
             n += w_cnt[w2];
             last = max(last, w_max[w2]);
         }
         __syncthreads();   // w_max / w_cnt are rewritten by the next round
     }
+    if (cnt == 0) {   // no round ran
+        grid_dep_wait();
+        for (int c = s * kSparseThreads + tid; c < p.num_counters; c += gridDim.x * kSparseThreads) p.counters[c] = 0;
+    }
     if (tid == 0) {
+        if (capped) flag_error(p.err, PKV_DEVERR_CAPACITY);
         if (any_bad) flag_error(p.err, PKV_DEVERR_PAGE_LIST);
         p.ctx_out[s] = n == 0 ? 0
                               : (last == npages - 1 ? kBlockSize * (n - 1) + (ctx - kBlockSize * (npages - 1))
