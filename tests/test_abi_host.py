@@ -36,6 +36,11 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), f"{n} missing from libpkv.so"
 
 
+def test_product_library_has_no_timeline_stamps(lib):
+    # the %globaltimer stamps (-DPKV_TIMELINE) live only in libpkv_timeline.so
+    assert not hasattr(lib, "pkv_timeline_attach")
+
+
 def test_status_strings(lib):
     for code, text in ((0, "ok"), (1, "invalid argument"), (2, "unsupported shape or type"), (3, "CUDA error")):
         assert lib.pkv_status_string(code).decode() == text
