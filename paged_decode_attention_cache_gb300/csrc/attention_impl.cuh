@@ -1384,7 +1384,10 @@ attention_kernel(const __grid_constant__ CUtensorMap k_map, const __grid_constan
                  const AttnParams p) {
     constexpr int NCW = Math::NCW;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1 KB aligned (the swizzled tiles need it), and derived from smem_raw by an
+    // offset so the compiler still knows every pointer below is shared memory
+    // (shared loads, not generic ones)
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     const int S = p.stages;
     const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL, D = p.head_dim;
     const int H = p.num_heads, Hkv = p.num_kv_heads;

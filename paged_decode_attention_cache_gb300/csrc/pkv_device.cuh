@@ -78,6 +78,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same test, letting the hardware suspend the thread for up to ns
+// nanoseconds until the phase completes (one instruction per wait instead of a
+// spin of tests that takes issue slots from the warps that have work).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, "
+        "p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Longest single suspension of a bounded wait (the timer is checked between them).
+constexpr uint32_t kWaitSuspendNs = 1u << 20;
+
 // Wait for the phase with the given parity to complete.  Returns false (and
 // the caller flags PKV_DEVERR_TIMEOUT) if it has not after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
@@ -85,9 +102,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(a, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait_suspend(a, parity, kWaitSuspendNs)) return true;
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
