@@ -251,8 +251,9 @@ struct CcMath {
                                                  const AttnParams&, int kvh, int pb, uint64_t* bar) {
         // byte-addressed maps, box = one kv head's 16 rows
         mbar_arrive_expect_tx(bar, TX);
-        tma_load_2d(dst, km, kvh * D * 2, pb * kBS, bar);
-        tma_load_2d(dst + KT, vm, kvh * D * 2, pb * kBS, bar);
+        const uint64_t pol = l2_evict_first_policy();
+        tma_load_2d_hint(dst, km, kvh * D * 2, pb * kBS, bar, pol);
+        tma_load_2d_hint(dst + KT, vm, kvh * D * 2, pb * kBS, bar, pol);
     }
 
     static constexpr bool kQ8 = false;
@@ -467,8 +468,9 @@ struct TcMath {
         // one 3-D box per tile: {128 bytes, 16 rows, D/64 chunks} lands as
         // D/64 consecutive 2 KB sub-tiles of 128-byte rows, 128B swizzle
         mbar_arrive_expect_tx(bar, TX);
-        tma_load_3d(dst, km, 0, pb * kBS, kvh * (D / 64), bar);
-        tma_load_3d(dst + OFF_V, vm, 0, pb * kBS, kvh * (D / 64), bar);
+        const uint64_t pol = l2_evict_first_policy();
+        tma_load_3d_hint(dst, km, 0, pb * kBS, kvh * (D / 64), bar, pol);
+        tma_load_3d_hint(dst + OFF_V, vm, 0, pb * kBS, kvh * (D / 64), bar, pol);
     }
 
     static constexpr bool kQ8 = false;
@@ -724,8 +726,9 @@ struct TqMath {
         }
         cp_async_mbar_arrive(bar);
         mbar_arrive_expect_tx(bar, TX);
-        tma_load_2d(dst, km, kvh * D, pb * kBS, bar);
-        tma_load_2d(dst + OFF_V, vm, kvh * (D / 2), pb * kBS, bar);
+        const uint64_t pol = l2_evict_first_policy();
+        tma_load_2d_hint(dst, km, kvh * D, pb * kBS, bar, pol);
+        tma_load_2d_hint(dst + OFF_V, vm, kvh * (D / 2), pb * kBS, bar, pol);
     }
 
     static constexpr bool kQ8 = true;
