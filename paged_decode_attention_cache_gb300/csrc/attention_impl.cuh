@@ -717,16 +717,16 @@ struct TqMath {
         const uint8_t* ks = reinterpret_cast<const uint8_t*>(p.k_scale) + meta * KS;
         const uint8_t* vs = reinterpret_cast<const uint8_t*>(p.v_scale) + meta * VS;
         const uint8_t* vz = reinterpret_cast<const uint8_t*>(p.v_zero) + meta * VS;
+        const uint64_t pol = l2_evict_first_policy();
 #pragma unroll
-        for (int c = 0; c < KS; c += 16) cp_async_16(dst + OFF_KS + c, ks + c);
+        for (int c = 0; c < KS; c += 16) cp_async_16_hint(dst + OFF_KS + c, ks + c, pol);
 #pragma unroll
         for (int c = 0; c < VS; c += 16) {
-            cp_async_16(dst + OFF_VS + c, vs + c);
-            cp_async_16(dst + OFF_VZ + c, vz + c);
+            cp_async_16_hint(dst + OFF_VS + c, vs + c, pol);
+            cp_async_16_hint(dst + OFF_VZ + c, vz + c, pol);
         }
         cp_async_mbar_arrive(bar);
         mbar_arrive_expect_tx(bar, TX);
-        const uint64_t pol = l2_evict_first_policy();
         tma_load_2d_hint(dst, km, kvh * D, pb * kBS, bar, pol);
         tma_load_2d_hint(dst + OFF_V, vm, kvh * (D / 2), pb * kBS, bar, pol);
     }

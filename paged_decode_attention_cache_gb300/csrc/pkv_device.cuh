@@ -175,6 +175,13 @@ __device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
 }
 
+// The same copy with an L2 cache policy (see l2_evict_first_policy).
+__device__ __forceinline__ void cp_async_16_hint(void* dst, const void* src, uint64_t pol) {
+    asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_addr(dst)), "l"(src),
+                 "l"(pol)
+                 : "memory");
+}
+
 // 16-byte shared-memory copy by explicit shared addresses.
 __device__ __forceinline__ void lds_sts_16(uint32_t dst, uint32_t src) {
     asm volatile(
