@@ -75,10 +75,17 @@ def analyse(rec: np.ndarray, n_launches: int, hkv: int):
         rows.append(np.stack([rel(rec[l, :, 0]), rel(rec[l, :, 1]), rel(rec[l, :, 2]), rel(rec[l, :, 3]),
                               rel(merged[l]), rel(end[l])], axis=-1))
     R = np.stack(rows)   # [launch, cta, phase]
-    return grid, R, np.array(periods), nseg[2:], blocks[2:], comb_end[2:]
+    # the last segment's end phases: merged -> published (pieces only) -> end
+    pub = np.where(nseg > 0, seg_t[idx_l, idx_c, last, 2], 0)
+    piece_end = ((rec[:, :, 28] >> (16 + last)) & 1).astype(bool) & (nseg > 0)
+    tails = {"merged_to_published": np.where(piece_end & (pub > 0), (pub - merged) / 1e3, np.nan)[2:],
+             "published_to_end": np.where(piece_end & (pub > 0), (end - pub) / 1e3, np.nan)[2:],
+             "merged_to_end": np.where(nseg > 0, (end - merged) / 1e3, np.nan)[2:],
+             "piece": piece_end[2:]}
+    return grid, R, np.array(periods), nseg[2:], blocks[2:], comb_end[2:], tails
 
 
-def report(workload, b, grid, R, periods, nseg, blocks, comb_end, hkv, flags):
+def report(workload, b, grid, R, periods, nseg, blocks, comb_end, hkv, flags, tails=None):
     out = []
     out.append(f"{workload} ({b.schedule}), grid {grid} = {grid // hkv} lane ranges x {hkv} kv heads; "
                f"{len(periods)} launches; device error flags {flags:#x}\n")
@@ -92,6 +99,19 @@ def report(workload, b, grid, R, periods, nseg, blocks, comb_end, hkv, flags):
         x = x[np.isfinite(x)]
         out.append(f"| {n} | {np.percentile(x, 10):.2f} | {np.median(x):.2f} | {x.max():.2f} |")
     out.append("")
+    if tails is not None:
+        out.append("| a CTA's last segment (µs, median) | CTAs | merged → published | published → end | merged → end |")
+        out.append("|---|---|---|---|---|")
+        kinds = (("whole (sequence, kv head) pair", ~tails["piece"]),
+                 ("piece, not the last of its pair", tails["piece"] & ~comb_end),
+                 ("piece that combines its pair", tails["piece"] & comb_end))
+        for name, sel in kinds:
+            if not sel.any():
+                continue
+            med = lambda a: f"{np.nanmedian(a[sel]):.2f}" if np.isfinite(a[sel]).any() else "–"
+            out.append(f"| {name} | {sel.sum() / len(sel):.0f} | {med(tails['merged_to_published'])} | "
+                       f"{med(tails['published_to_end'])} | {med(tails['merged_to_end'])} |")
+        out.append("")
     out.append("| lane range | segments | blocks | combines at its end | first copies | last blocks merged | end |")
     out.append("|---|---|---|---|---|---|---|")
     nl = grid // hkv
@@ -112,8 +132,8 @@ def main(argv=None):
     steps = min(a.steps, LAUNCHES)
     b, rec, n_entries, flags = record(a.workload, steps)
     hkv = b.w.num_kv_heads
-    grid, R, periods, nseg, blocks, comb_end = analyse(rec, steps, hkv)
-    print(report(a.workload, b, grid, R, periods, nseg, blocks, comb_end, hkv, flags))
+    grid, R, periods, nseg, blocks, comb_end, tails = analyse(rec, steps, hkv)
+    print(report(a.workload, b, grid, R, periods, nseg, blocks, comb_end, hkv, flags, tails))
     return 0
 
 

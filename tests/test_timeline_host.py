@@ -24,7 +24,7 @@ def _record(n_launches=4, grid=4):
 
 
 def test_phases_are_relative_to_the_previous_launchs_last_cta():
-    grid, R, periods, nseg, blocks, comb_end = T.analyse(_record(), 4, hkv=2)
+    grid, R, periods, nseg, blocks, comb_end, tails = T.analyse(_record(), 4, hkv=2)
     assert grid == 4
     # launches 2 and 3 are reported; the last CTA (1: two segments) ends at t0 + 12_100
     assert R.shape == (2, 4, 6)
@@ -36,16 +36,24 @@ def test_phases_are_relative_to_the_previous_launchs_last_cta():
     assert (nseg[:, 1] == 2).all() and (nseg[:, 0] == 1).all()
     assert (blocks[:, 1] == 60).all() and (blocks[:, 0] == 60).all()
     assert comb_end[:, 2].all() and not comb_end[:, 0].any()
+    # the piece bit is set for segment 0 only: CTA 1's last (second) segment is a whole pair;
+    # merged at 6_000 + 5_000 k, published 500 later, end 1_000 + 100 c after the merge
+    assert tails["piece"][:, [0, 2, 3]].all() and not tails["piece"][:, 1].any()
+    assert np.allclose(tails["merged_to_published"][:, [0, 2, 3]], 0.5)
+    assert np.isnan(tails["merged_to_published"][:, 1]).all()
+    assert np.allclose(tails["published_to_end"][:, 3], 0.8)
+    assert np.allclose(tails["merged_to_end"][:, 1], 1.1)
 
 
 def test_report_lists_every_lane_range():
     rec = _record()
-    grid, R, periods, nseg, blocks, comb_end = T.analyse(rec, 4, hkv=2)
+    grid, R, periods, nseg, blocks, comb_end, tails = T.analyse(rec, 4, hkv=2)
 
     class B:
         schedule = "balanced"
 
-    text = T.report("w", B(), grid, R, periods, nseg, blocks, comb_end, 2, 0)
+    text = T.report("w", B(), grid, R, periods, nseg, blocks, comb_end, 2, 0, tails)
     rows = [l for l in text.splitlines() if l.startswith("| 0 |") or l.startswith("| 1 |")]
     assert len(rows) == 2
     assert "Launch period" in text
+    assert "piece that combines its pair" in text
