@@ -52,16 +52,9 @@ METRIC = "paged-decode attention KV-read GB/s (% of HBM peak); decode steps/sec"
 GRAPH_MAX_STEPS = 1000
 SLEEP_CYCLES = 400_000   # ~0.2 ms of spinning ahead of each timed region
 
-WORKLOADS = {
-    "tiny_f16": 1,
-    "llama3_8b_batch8": 2,
-    "long_context_32k": 3,
-    "k8v4_batch32": 4,
-    "verify_batch256": 5,
-    "sliding_window_b8_w4096": "sliding_window_b8_w4096",
-    "cascade_b32_p2048": "cascade_b32_p2048",
-    "sparse_b4_32k": "sparse_b4_32k",
-}
+WORKLOADS = ["tiny_f16", "llama3_8b_batch8", "long_context_32k", "k8v4_batch32", "verify_batch256",
+             "sliding_window_b8_w4096", "cascade_b32_p2048", "sparse_b4_32k"]
+# the five decode / verify workloads reported in per_config
 CONFIG_ORDER = ["tiny_f16", "llama3_8b_batch8", "long_context_32k", "k8v4_batch32", "verify_batch256"]
 DEFAULT_WORKLOAD = "llama3_8b_batch8"
 # schedule of the attention call per workload: the decode ones run the whole
@@ -155,8 +148,7 @@ def summary(times):
 
 def make_workload(name, device, seed_offset=0, partition=None):
     from paged_decode_attention_cache_gb300 import workloads as W
-    key = WORKLOADS[name]
-    fn = W.CONFIGS[key] if isinstance(key, int) else W.EXTRA[key]
+    fn = W.BY_NAME[name]
     kw = {}
     if partition is not None and name != "tiny_f16":
         kw["partition_size"] = partition

@@ -348,8 +348,9 @@ def sparse_b4_32k(device="cpu", seed=8) -> Workload:
     return w
 
 
-CONFIGS = {1: tiny_f16, 2: llama3_8b_batch8, 3: long_context_32k, 4: k8v4_batch32,
-           5: verify_batch256}
-# workloads beyond the five configurations (rows ranked next)
-EXTRA = {"sliding_window_b8_w4096": sliding_window_b8_w4096, "cascade_b32_p2048": cascade_b32_p2048,
-         "sparse_b4_32k": sparse_b4_32k}
+# every workload by name: the five decode / verify workloads of the scope, then
+# those of the rows ranked next (windows, cascade prefixes, sparse page lists)
+BY_NAME = {"tiny_f16": tiny_f16, "llama3_8b_batch8": llama3_8b_batch8, "long_context_32k": long_context_32k,
+           "k8v4_batch32": k8v4_batch32, "verify_batch256": verify_batch256,
+           "sliding_window_b8_w4096": sliding_window_b8_w4096, "cascade_b32_p2048": cascade_b32_p2048,
+           "sparse_b4_32k": sparse_b4_32k}
