@@ -58,7 +58,7 @@ def run_step(w, partition=None, out_dtype=torch.float32):
     return st, out.double().cpu().numpy()
 
 
-# ---------------------------------------------------------------- config 1
+# ---------------------------------------------------------------- tiny fp16 step (64 tokens, 4 / 2 heads)
 
 def test_tiny_f16_full_step():
     w = W.tiny_f16()
