@@ -656,6 +656,202 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
     return r;
 }
 
+// fp16 / bf16 cache, up to 8 query rows per kv head (decode at group size 4
+// and 8, verify blocks of g * q_len <= 8).  The same tiles as TcMath, with the
+// contraction turned around as for K8/V4: S^T = K Q^T puts the block's 16
+// tokens on the MMA's M side and the query rows on its 8 columns, and
+// O^T = V^T P^T puts 16 head dims on M.  Per 16-token block that is D/16 MMAs
+// for the scores and D/16 for the values (twice that for P's low bf16 half),
+// where a 16-row query tile spends as many on 12 padding rows.
+//   K: the A operand straight from the swizzled tile (ldmatrix).
+//   V: the A operand V^T from the tile (ldmatrix.trans); rows past the
+//      context are zeroed in the operand (they may hold NaN).
+//   P: the S^T accumulator is packed and turned into the P^T operand with
+//      movmatrix; bf16 keeps 8 significant bits, so P = hi + lo (two MMAs, P
+//      exact to ~2^-17), fp16's 11 bits are kept as one operand.
+template <int KIND, int D>
+struct TtMath {
+    static constexpr bool kTensor = true;
+    static constexpr int kD = D;
+    static constexpr int NCW = 7;
+    static constexpr int kSegCost = pkv::kSegCost;
+    static constexpr int kIssueGroup = 8;
+    static constexpr bool BF = KIND == PKV_CACHE_BF16;
+    static constexpr int NKS = D / 16;     // k-steps of the score contraction
+    static constexpr int NMT = D / 16;     // M tiles of O^T
+    static constexpr int KT = kBS * 2 * D;
+    static constexpr int VT = kBS * 2 * D;
+    static constexpr int OFF_V = align_up(KT, 1024);
+    static constexpr int TX = KT + VT;   // bytes the TMA copies deliver
+    static constexpr int STAGE = align_up(OFF_V + VT, 1024);
+    static constexpr int SCRATCH = 0;
+    static_assert(KIND != PKV_CACHE_K8V4, "K8/V4 runs TqMath");
+    static_assert(OFF_V % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1 KB alignment");
+
+    uint32_t qb[NKS][2];   // Q^T operand: query column g, this thread's dims
+    float o[NMT][4];       // O^T: dims (g, g + 8) of each M tile x query columns (2t, 2t + 1)
+    float m_run[2], l_part[2];   // query columns 2t, 2t + 1 (l: this thread's tokens)
+    int lim[2];
+    int lo_;   // first visible token (sliding window)
+    float scale_log2_;
+
+    static __device__ __forceinline__ void issue(uint8_t* dst, const CUtensorMap* km, const CUtensorMap* vm,
+                                                 const AttnParams& p, int kvh, int pb, uint64_t* bar) {
+        TcMath<KIND, D>::issue(dst, km, vm, p, kvh, pb, bar);
+    }
+
+    static constexpr bool kQ8 = false;
+    __device__ __forceinline__ void patch(uint8_t* stg, int r, int j, const uint8_t* buf, int lane,
+                                          const AttnParams& p) const {
+        constexpr int CHK = D * 2 / 16;
+        if (lane < 2 * CHK) {
+            const int c = lane % CHK;
+            lds_sts_16(smem_addr(stg) + (lane < CHK ? 0 : OFF_V) + (c >> 3) * 2048 + r * 128 + 16 * swz<128>(c & 7, r),
+                       smem_addr(buf) + j * 4 * D + 16 * lane);
+        }
+    }
+
+    __device__ __forceinline__ void init(int) {}
+
+    // query column n = row m of the pair (head m / q_len, draft m % q_len)
+    template <bool CASC>
+    __device__ __forceinline__ void begin(const AttnParams& p, int s, int kvh, int ctx, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+        const int G = p.num_heads / p.num_kv_heads, QL = p.q_len, M = G * QL;
+        lo_ = visible_lo<CASC>(p, s, ctx);
+        {
+            // this thread's B fragments: column g
+            const int h = g < M ? g / QL : 0, j = g < M ? g % QL : 0;
+            const int qr = g < M ? query_row<CASC>(p, s, j) : -1;
+            const bool valid = qr >= 0;
+            const size_t qoff = (size_t(valid ? qr : 0) * p.num_heads + kvh * G + h) * D;
+            const uint32_t* qw = reinterpret_cast<const uint32_t*>(p.q);
+#pragma unroll
+            for (int kk = 0; kk < NKS; ++kk) {
+                qb[kk][0] = valid ? qw[(qoff + 16 * kk + 2 * t) / 2] : 0u;
+                qb[kk][1] = valid ? qw[(qoff + 16 * kk + 8 + 2 * t) / 2] : 0u;
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            // this thread's accumulator columns 2t + e
+            const int n = 2 * t + e;
+            const int j = n < M ? n % QL : 0;
+            const bool ok = n < M && query_row<CASC>(p, s, j) >= 0;
+            // a cascade row (one decode query) sees the entry's whole context; verify rows are causal
+            lim[e] = ok ? (CASC ? ctx : max(0, ctx - QL + j + 1)) : 0;
+            m_run[e] = -INFINITY;
+            l_part[e] = 0.f;
+        }
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    }
+
+    __device__ __forceinline__ void block(const uint8_t* stg, int pos0, int ntok, uint8_t*, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+        const int mi = lane >> 3, r = lane & 7;
+        const uint32_t stg_a = smem_addr(stg);
+        // ------------------------------------------------ S^T = K Q^T (rows = tokens g, g + 8)
+        float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < NKS; ++kk) {
+            // matrices: tokens 0-7 / 8-15 of 8-dim chunk 2kk, then of chunk 2kk + 1
+            const int tk = (mi & 1) * 8 + r, c = 2 * kk + (mi >> 1);
+            uint32_t a[4];
+            ldsm_x4(stg_a + (c >> 3) * 2048 + tk * 128 + 16 * swz<128>(c & 7, tk), a);
+            mma16816<BF>(sc, a, qb[kk][0], qb[kk][1]);
+        }
+        // scale, context / causal / window mask
+        const int pg = pos0 + g, pg8 = pos0 + g + 8;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            sc[e] = (pg < lim[e] && pg >= lo_) ? sc[e] * scale_log2_ : -INFINITY;
+            sc[2 + e] = (pg8 < lim[e] && pg8 >= lo_) ? sc[2 + e] * scale_log2_ : -INFINITY;
+        }
+        // ------------------------------------------------ online softmax per query column
+        float alpha[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float bm = fmaxf(sc[e], sc[2 + e]);
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 4));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 8));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 16));
+            const float mn = fmaxf(m_run[e], bm);
+            const float mu = (mn == -INFINITY) ? 0.f : mn;
+            // nothing accumulated yet (padding columns stay so): no rescale
+            alpha[e] = (m_run[e] == -INFINITY) ? 1.f : exp2f(m_run[e] - mu);
+            const float p0 = exp2f(sc[e] - mu), p1 = exp2f(sc[2 + e] - mu);
+            sc[e] = p0;
+            sc[2 + e] = p1;
+            l_part[e] = l_part[e] * alpha[e] + (p0 + p1);
+            m_run[e] = mn;
+        }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < NMT; ++mt) {
+                o[mt][0] *= alpha[0]; o[mt][2] *= alpha[0];
+                o[mt][1] *= alpha[1]; o[mt][3] *= alpha[1];
+            }
+        }
+        // ------------------------------------------------ P^T operand (tokens 2t.., query column g)
+        const uint32_t p01 = pack2<BF>(sc[0], sc[1]), p23 = pack2<BF>(sc[2], sc[3]);
+        const uint32_t b0 = movm_trans(p01), b1 = movm_trans(p23);
+        uint32_t c0 = 0u, c1 = 0u;
+        if constexpr (BF) {
+            const uint32_t l01 = pack2<BF>(sc[0] - __uint_as_float(p01 << 16), sc[1] - __uint_as_float(p01 & 0xffff0000u));
+            const uint32_t l23 = pack2<BF>(sc[2] - __uint_as_float(p23 << 16), sc[3] - __uint_as_float(p23 & 0xffff0000u));
+            c0 = movm_trans(l01);
+            c1 = movm_trans(l23);
+        }
+        // V rows past the context may hold anything (NaN): zero them in the operand
+        const uint32_t m01 = (2 * t < ntok ? 0x0000ffffu : 0u) | (2 * t + 1 < ntok ? 0xffff0000u : 0u);
+        const uint32_t m23 = (8 + 2 * t < ntok ? 0x0000ffffu : 0u) | (9 + 2 * t < ntok ? 0xffff0000u : 0u);
+        // ------------------------------------------------ O^T += V^T P^T
+#pragma unroll
+        for (int mt = 0; mt < NMT; ++mt) {
+            // matrices (transposed): tokens 0-7 of chunks 2mt, 2mt + 1, then tokens 8-15
+            const int tk = (mi >> 1) * 8 + r, c = 2 * mt + (mi & 1);
+            uint32_t a[4];
+            ldsm_x4_t(stg_a + OFF_V + (c >> 3) * 2048 + tk * 128 + 16 * swz<128>(c & 7, tk), a);
+            if (ntok < kBS) {
+                a[0] &= m01; a[1] &= m01; a[2] &= m23; a[3] &= m23;
+            }
+            mma16816<BF>(o[mt], a, b0, b1);
+            if constexpr (BF) mma16816<BF>(o[mt], a, c0, c1);
+        }
+    }
+
+    __device__ __forceinline__ void finish(int) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float l = l_part[e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            l_part[e] = l;
+        }
+    }
+
+    // unnormalised rows [M][D] (ob_idx order) and per-row (m, l) of this warp
+    __device__ __forceinline__ void store(float* ob, float* mw, float* lw, int M, int lane) const {
+        const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const int q = 2 * t + e;
+            if (q >= M) continue;
+#pragma unroll
+            for (int mt = 0; mt < NMT; ++mt) {
+                ob[ob_idx(q, 16 * mt + g, D)] = o[mt][e];
+                ob[ob_idx(q, 16 * mt + g + 8, D)] = o[mt][2 + e];
+            }
+            if (g == 0) {
+                mw[q] = m_run[e];
+                lw[q] = l_part[e];
+            }
+        }
+    }
+};
+
 // K8/V4 cache (see quantize_kernel).  The query tile of a decode block is only
 // g*q_len rows, so the contraction is turned around: S^T = K Q^T puts the 16
 // tokens on the MMA's M side and up to 8 (NT = 1) or 16 (NT = 2) query columns
@@ -1921,9 +2117,15 @@ cudaError_t launch_attention_impl(const AttnParams& p, int cache_kind, int gqa, 
                               : launch_math<TqMath<64, 2>, FUSED, CASC>(p, km, vm, stream);
             }
             case PKV_CACHE_BF16:
+                if ((p.num_heads / p.num_kv_heads) * p.q_len <= 8)
+                    return p.head_dim == 128 ? launch_math<TtMath<PKV_CACHE_BF16, 128>, FUSED, CASC>(p, km, vm, stream)
+                                             : launch_math<TtMath<PKV_CACHE_BF16, 64>, FUSED, CASC>(p, km, vm, stream);
                 return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_BF16, 128>, FUSED, CASC>(p, km, vm, stream)
                                          : launch_math<TcMath<PKV_CACHE_BF16, 64>, FUSED, CASC>(p, km, vm, stream);
             default:
+                if ((p.num_heads / p.num_kv_heads) * p.q_len <= 8)
+                    return p.head_dim == 128 ? launch_math<TtMath<PKV_CACHE_F16, 128>, FUSED, CASC>(p, km, vm, stream)
+                                             : launch_math<TtMath<PKV_CACHE_F16, 64>, FUSED, CASC>(p, km, vm, stream);
                 return p.head_dim == 128 ? launch_math<TcMath<PKV_CACHE_F16, 128>, FUSED, CASC>(p, km, vm, stream)
                                          : launch_math<TcMath<PKV_CACHE_F16, 64>, FUSED, CASC>(p, km, vm, stream);
         }
