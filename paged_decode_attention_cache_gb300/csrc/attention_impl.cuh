@@ -38,9 +38,12 @@
 //   CcMath  fp16/bf16 decode at group size 1 or 2, CUDA cores: fp32 q pairs,
 //           packed fma.rn.f32x2, reduce-scatter shuffles, softmax over 16 x g
 //           scores in shared memory;
-//   TcMath  fp16/bf16 whenever a kv head serves >= 4 query rows (decode at
-//           group size 4 and 8, verify blocks): mma.sync m16n8k16 on 16 query
-//           rows (g heads x q_len drafts), 128B-swizzled tiles via ldmatrix;
+//   TtMath  fp16/bf16 when a kv head serves 4 to 8 query rows (decode at
+//           group size 4 and 8, verify blocks of up to 8 rows): mma.sync
+//           m16n8k16 with the contraction turned around (S^T = K Q^T,
+//           O^T = V^T P^T), 128B-swizzled tiles via ldmatrix;
+//   TcMath  fp16/bf16 for 9 to 16 query rows (the wider verify blocks):
+//           mma.sync m16n8k16 on 16 query rows (g heads x q_len drafts);
 //   TqMath  K8/V4, any q_len: the contraction turned around (S^T = K Q^T,
 //           O^T = V^T P^T) so the query columns sit on the MMA's N side; codes
 //           become exact fp16 integers in registers.
