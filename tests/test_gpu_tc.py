@@ -42,9 +42,13 @@ def run(w, part, out_dtype=torch.float32):
 
 # ---------------------------------------------------------------- verify (q_len > 1)
 
+# query rows per kv head (g * q_len): 16 (the 16-row tile), 8, 6 and 5 (the
+# transposed tile, padding columns at 6 and 5), 3 (CUDA cores), and group size
+# 8 decode (the transposed tile, 8 columns)
 VERIFY = []
 for D in (64, 128):
-    for H, Hkv, ql in ((8, 2, 4), (32, 8, 4), (4, 4, 16), (16, 2, 2), (8, 8, 3), (16, 2, 1)):
+    for H, Hkv, ql in ((8, 2, 4), (32, 8, 4), (4, 4, 16), (16, 2, 2), (8, 2, 2), (8, 4, 3), (4, 4, 5), (8, 8, 3),
+                       (16, 2, 1)):
         VERIFY.append((D, H, Hkv, ql))
 
 
@@ -52,8 +56,6 @@ for D in (64, 128):
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
 @pytest.mark.parametrize("part", [0, 32, 512, "bal"])
 def test_verify_small(D, H, Hkv, ql, dt, part):
-    if ql == 1 and part in (512, "bal"):
-        pytest.skip("q_len 1 on fp16/bf16 runs the CUDA-core kernel")
     ctx = [2, 3, 4, 5, 16, 17, 100, 513]
     w = W.build(name="t", seed=200 + D + H + ql, context_lens=ctx, num_heads=H, num_kv_heads=Hkv, head_dim=D,
                 cache=dt, q_len=ql)
