@@ -57,6 +57,9 @@ CASES = [
     ("f16", 8, 1, 128, 1, "free", 0),
     ("bf16", 8, 2, 128, 4, "tail", 0),
     ("f16", 16, 8, 64, 2, "tail", 0),
+    ("bf16", 8, 2, 128, 2, "tail", 0),
+    ("bf16", 4, 2, 128, 3, "tail", 0),
+    ("f16", 16, 2, 64, 1, "tail", 0),
     ("bf16", 8, 2, 128, 4, "tail", 48),
     ("k8v4", 8, 2, 128, 1, "tail", 0),
     ("k8v4", 32, 8, 128, 1, "tail", 0),
