@@ -424,17 +424,23 @@ def e2e_measure(bench, K, device, ws):
     """The same step through the public API with host buffers, run as a serving
     loop runs it: every step's inputs are packed in a pinned host buffer and
     copied in with one host-to-device transfer, the step is launched, and its
-    output is copied back to pinned host memory.  Two replicas alternate, so one
-    step's copies overlap the other's kernels: copies in on one stream, steps on
-    the capture stream, copies out on a third; events put each step after its
-    inputs' copy and after the copy-out of the step that last used its output,
-    and each copy-in after the step that last read that buffer.  The loop is
-    captured in CUDA graphs like the device-timed steps (eager launches would
-    time the host's enqueue rate instead)."""
+    output is copied back to pinned host memory.  Independent replicas (request
+    groups) are served in two banks of G that alternate, so one bank's copies
+    overlap the other bank's kernels: a bank's G copies in on one stream, its G
+    steps back to back on the capture stream, their copies out on a third;
+    events put a bank's steps after its inputs' copies and after the copies out
+    of its previous steps, and its copies in after its previous steps.  Only
+    the first step of a bank waits on a copy: a kernel that depends on a copy
+    is not launched under the previous kernel's tail (programmatic dependent
+    launch), so each wait costs a step the full grid-completion hop.  The loop
+    is captured in CUDA graphs like the device-timed steps (eager launches
+    would time the host's enqueue rate instead)."""
     import torch
+    G = max(1, min(4, bench.reps // 2))   # replicas per bank
+    NR = 2 * G
     pairs = []
-    for r in range(2):
-        st = bench.steps[r % bench.reps]
+    for r in range(NR):
+        st = bench.steps[r]
         schedule = bench.schedule
         src = [st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens]
         if schedule == "cascade":
@@ -461,7 +467,7 @@ def e2e_measure(bench, K, device, ws):
         pairs.append((st, host_buf, dev_buf, host_out))
     h2d = pairs[0][2].numel()
     d2h = pairs[0][3].numel() * pairs[0][3].element_size()
-    Ke = max(10, min(K, 500)) // 2 * 2
+    Ke = max(2 * NR, min(K, 500)) // NR * NR   # whole cycles of both banks
     h2d_s, d2h_s = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
     def capture(n):
@@ -475,35 +481,41 @@ def e2e_measure(bench, K, device, ws):
             ev_in = [torch.cuda.Event() for _ in range(2)]
             ev_done = [torch.cuda.Event() for _ in range(2)]
             ev_out = [torch.cuda.Event() for _ in range(2)]
-            for k in range(n):
-                r = k & 1
-                st, hb, db, ho = pairs[r]
-                if k >= 2:
-                    h2d_s.wait_event(ev_done[r])   # the step two back has read this buffer
+            nb = n // G
+            for j in range(nb):
+                b = j & 1
+                bank = pairs[b * G:(b + 1) * G]
+                if j >= 2:
+                    h2d_s.wait_event(ev_done[b])   # the bank's previous steps have read these buffers
                 with torch.cuda.stream(h2d_s):
-                    db.copy_(hb, non_blocking=True)
-                    ev_in[r].record(h2d_s)
-                cap.wait_event(ev_in[r])
-                if k >= 2:
-                    cap.wait_event(ev_out[r])      # its output has been copied out
-                st.step(cap)
-                ev_done[r].record(cap)
-                d2h_s.wait_event(ev_done[r])
+                    for st, hb, db, ho in bank:
+                        db.copy_(hb, non_blocking=True)
+                    ev_in[b].record(h2d_s)
+                cap.wait_event(ev_in[b])
+                if j >= 2:
+                    cap.wait_event(ev_out[b])      # their outputs have been copied out
+                for st, hb, db, ho in bank:
+                    st.step(cap)
+                ev_done[b].record(cap)
+                d2h_s.wait_event(ev_done[b])
                 with torch.cuda.stream(d2h_s):
-                    ho.copy_(st.out, non_blocking=True)
-                    ev_out[r].record(d2h_s)
-            cap.wait_event(ev_in[(n - 1) & 1])
+                    for st, hb, db, ho in bank:
+                        ho.copy_(st.out, non_blocking=True)
+                    ev_out[b].record(d2h_s)
+            cap.wait_event(ev_in[(nb - 1) & 1])
             cap.wait_event(ev_out[0])
             cap.wait_event(ev_out[1])
         return g
 
-    graphs = [capture(n) for n in [min(GRAPH_MAX_STEPS, Ke - k) for k in range(0, Ke, GRAPH_MAX_STEPS)]]
+    per_graph = max(NR, GRAPH_MAX_STEPS // NR * NR)
+    graphs = [capture(n) for n in [min(per_graph, Ke - k) for k in range(0, Ke, per_graph)]]
     times = time_graphs(graphs, Ke, 3, device, ws)
     e2e_ms = sorted(times)[len(times) // 2]
     return {"value": job_throughput(ws, bench.total_b, e2e_ms), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "steps": Ke,
-            "how": "pinned host inputs copied in and the output copied back every step, two replicas "
-                   "alternating so copies overlap the other replica's kernels, captured in CUDA graphs"}
+            "how": f"pinned host inputs copied in and the output copied back every step; two banks of {G} "
+                   "independent replicas alternate so one bank's copies overlap the other's kernels, and "
+                   "a bank's steps run back to back; captured in CUDA graphs"}
 
 
 # ---------------------------------------------------------------- the oracle on the host
