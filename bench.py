@@ -436,11 +436,16 @@ def e2e_measure(bench, K, device, ws):
     is captured in CUDA graphs like the device-timed steps (eager launches
     would time the host's enqueue rate instead)."""
     import torch
-    G = max(1, min(4, bench.reps // 2))   # replicas per bank
+    from paged_decode_attention_cache_gb300.runner import DecodeStep
+    # replicas per bank: 4 when eight copies of the step's data stay small (extra
+    # replicas are made for it), else as many as the device-timed rotation holds
+    G = 4 if 8 * bench.total_b <= (1 << 31) else max(1, min(4, bench.reps // 2))
     NR = 2 * G
+    steps = list(bench.steps[:NR]) + [DecodeStep(bench.w, device, schedule=bench.schedule)
+                                      for _ in range(NR - min(NR, bench.reps))]
     pairs = []
     for r in range(NR):
-        st = bench.steps[r]
+        st = steps[r]
         schedule = bench.schedule
         src = [st.q, st.k_new, st.v_new, st.slot_new, st.seqs.block_tables, st.seqs.context_lens]
         if schedule == "cascade":
